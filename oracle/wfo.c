@@ -1,0 +1,233 @@
+/*
+ * wfo.c -- fp64 CPU oracle for attention over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE (see wfo.h for who may use it and for
+ * the passages each function follows).  Plain loops, fp64, no blocking, no
+ * online softmax, no reordering: a reader can hold it against the definition.
+ *
+ * Threads only split the independent (query row, head) outputs; every output
+ * is computed by one thread in one fixed order, so results do not depend on
+ * the thread count.
+ */
+#include "wfo.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- exact widening of a stored element to double -------------------- */
+static double load_elem(const void* base, int64_t idx, int dtype) {
+    if (dtype == WFO_F32) {
+        float f;
+        memcpy(&f, (const char*)base + idx * 4, 4);
+        return (double)f;
+    } else {
+        uint16_t h;
+        uint32_t u;
+        float f;
+        memcpy(&h, (const char*)base + idx * 2, 2);
+        u = ((uint32_t)h) << 16; /* bfloat16 is the top half of a float32 */
+        memcpy(&f, &u, 4);
+        return (double)f;
+    }
+}
+
+static int elem_bytes(int dtype) { return dtype == WFO_F32 ? 4 : 2; }
+
+/* ---- scatter (weft "Cache layouts": write = scatter via slot_mapping) -- */
+int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                          const int64_t* slot_mapping, int64_t T,
+                          int64_t N, int64_t P, int64_t H_kv, int64_t D, int dtype) {
+    if ((dtype != WFO_F32 && dtype != WFO_BF16) || T < 0 || N < 1 || P < 1 || H_kv < 1 || D < 1)
+        return WFO_ERR_ARG;
+    const int64_t row_bytes = H_kv * D * elem_bytes(dtype);
+    /* validate everything before writing anything */
+    for (int64_t t = 0; t < T; ++t)
+        if (slot_mapping[t] >= N * P) return WFO_ERR_SLOT;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue; /* padding token: nothing to write */
+        const int64_t block = slot / P;
+        const int64_t offset = slot % P;
+        const int64_t dst = (block * P + offset) * row_bytes;
+        memcpy((char*)k_pool + dst, (const char*)k + t * row_bytes, (size_t)row_bytes);
+        memcpy((char*)v_pool + dst, (const char*)v + t * row_bytes, (size_t)row_bytes);
+    }
+    return 0;
+}
+
+/* ---- one attention row: softmax over positions 0..len-1 of one sequence -- */
+typedef struct {
+    const void* q;          /* query rows [rows, H_q, D]          */
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* row_req;  /* query row -> request               */
+    const int32_t* row_len;  /* query row -> number of positions   */
+    int64_t rows, M, H_q, H_kv, D, N, P;
+    double scale;
+    int dtype;
+    double* out;
+    int64_t next;            /* shared work counter (atomic)       */
+    int status;
+} job_t;
+
+/* out_row[d] = sum_p w_p V_p[d] / sum_p w_p with w_p = exp(s_p - max_p s_p),
+ * s_p = scale * sum_d q[d] K_p[d]; K_p, V_p read at block_table[p / P],
+ * offset p % P, KV head h. */
+static int attend_row(const job_t* J, int64_t row, int64_t g, double* s, double* acc) {
+    const int64_t b = J->row_req[row];
+    const int64_t len = J->row_len[row];
+    const int64_t G = J->H_q / J->H_kv;
+    const int64_t h = g / G;
+    const int64_t qbase = (row * J->H_q + g) * J->D;
+    const int32_t* table = J->block_tables + b * J->M;
+    double m = -INFINITY;
+    for (int64_t p = 0; p < len; ++p) {
+        const int64_t block = table[p / J->P];
+        const int64_t offset = p % J->P;
+        if (block < 0 || block >= J->N) return WFO_ERR_BLOCK;
+        const int64_t kbase = ((block * J->P + offset) * J->H_kv + h) * J->D;
+        double dot = 0.0;
+        for (int64_t d = 0; d < J->D; ++d)
+            dot += load_elem(J->q, qbase + d, J->dtype) * load_elem(J->k_pool, kbase + d, J->dtype);
+        s[p] = J->scale * dot;
+        if (s[p] > m) m = s[p];
+    }
+    double den = 0.0;
+    for (int64_t d = 0; d < J->D; ++d) acc[d] = 0.0;
+    for (int64_t p = 0; p < len; ++p) {
+        const double w = exp(s[p] - m);
+        const int64_t block = table[p / J->P];
+        const int64_t offset = p % J->P;
+        const int64_t vbase = ((block * J->P + offset) * J->H_kv + h) * J->D;
+        den += w;
+        for (int64_t d = 0; d < J->D; ++d) acc[d] += w * load_elem(J->v_pool, vbase + d, J->dtype);
+    }
+    double* o = J->out + (row * J->H_q + g) * J->D;
+    for (int64_t d = 0; d < J->D; ++d) o[d] = acc[d] / den;
+    return 0;
+}
+
+static void* worker(void* arg) {
+    job_t* J = (job_t*)arg;
+    int64_t maxlen = 1;
+    for (int64_t r = 0; r < J->rows; ++r)
+        if (J->row_len[r] > maxlen) maxlen = J->row_len[r];
+    double* s = (double*)malloc(sizeof(double) * (size_t)maxlen);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)J->D);
+    if (!s || !acc) {
+        __atomic_store_n(&J->status, WFO_ERR_MEM, __ATOMIC_RELAXED);
+        free(s);
+        free(acc);
+        return NULL;
+    }
+    const int64_t total = J->rows * J->H_q;
+    for (;;) {
+        const int64_t item = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (item >= total) break;
+        const int rc = attend_row(J, item / J->H_q, item % J->H_q, s, acc);
+        if (rc) __atomic_store_n(&J->status, rc, __ATOMIC_RELAXED);
+    }
+    free(s);
+    free(acc);
+    return NULL;
+}
+
+static int run_job(job_t* J, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    J->next = 0;
+    J->status = 0;
+    if (nthreads == 1) {
+        worker(J);
+        return J->status;
+    }
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th) return WFO_ERR_MEM;
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, worker, J) != 0) break;
+        ++started;
+    }
+    if (started == 0) worker(J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    return J->status;
+}
+
+static int check_common(const int32_t* block_tables, int64_t M, int64_t B, int64_t H_q,
+                        int64_t H_kv, int64_t D, int64_t N, int64_t P, int dtype) {
+    if ((dtype != WFO_F32 && dtype != WFO_BF16) || B < 0 || M < 1 || H_q < 1 || H_kv < 1 ||
+        D < 1 || N < 1 || P < 1 || H_q % H_kv != 0)
+        return WFO_ERR_ARG;
+    (void)block_tables;
+    return 0;
+}
+
+/* ---- decode (one query per sequence; attends to all its positions) ---- */
+int wfo_paged_decode(double* out, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
+                     int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
+                     double scale, int dtype, int nthreads) {
+    int rc = check_common(block_tables, M, B, H_q, H_kv, D, N, P, dtype);
+    if (rc) return rc;
+    for (int64_t b = 0; b < B; ++b)
+        if (seq_lens[b] < 1 || seq_lens[b] > M * P) return WFO_ERR_LEN;
+    int32_t* row_req = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    int32_t* row_len = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    if (!row_req || !row_len) {
+        free(row_req);
+        free(row_len);
+        return WFO_ERR_MEM;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        row_req[b] = (int32_t)b;
+        row_len[b] = seq_lens[b];
+    }
+    job_t J = {q, k_pool, v_pool, block_tables, seq_lens, row_req, row_len,
+               B, M, H_q, H_kv, D, N, P, scale, dtype, out, 0, 0};
+    rc = run_job(&J, nthreads);
+    free(row_req);
+    free(row_len);
+    return rc;
+}
+
+/* ---- prefill (causal varlen over the cached prefix plus the new rows) --- */
+int wfo_paged_prefill(double* out, const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
+                      const int32_t* cu_q_lens, int64_t B, int64_t H_q, int64_t H_kv,
+                      int64_t D, int64_t N, int64_t P, double scale, int dtype, int nthreads) {
+    int rc = check_common(block_tables, M, B, H_q, H_kv, D, N, P, dtype);
+    if (rc) return rc;
+    if (cu_q_lens[0] != 0) return WFO_ERR_ARG;
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t n = (int64_t)cu_q_lens[b + 1] - cu_q_lens[b];
+        if (n < 0) return WFO_ERR_ARG;
+        if (seq_lens[b] < n || seq_lens[b] > M * P || (n > 0 && seq_lens[b] < 1)) return WFO_ERR_LEN;
+    }
+    const int64_t rows = cu_q_lens[B];
+    int32_t* row_req = (int32_t*)malloc(sizeof(int32_t) * (size_t)(rows > 0 ? rows : 1));
+    int32_t* row_len = (int32_t*)malloc(sizeof(int32_t) * (size_t)(rows > 0 ? rows : 1));
+    if (!row_req || !row_len) {
+        free(row_req);
+        free(row_len);
+        return WFO_ERR_MEM;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t n = (int64_t)cu_q_lens[b + 1] - cu_q_lens[b];
+        const int64_t c = seq_lens[b] - n; /* cached prefix length */
+        for (int64_t i = 0; i < n; ++i) {
+            row_req[cu_q_lens[b] + i] = (int32_t)b;
+            row_len[cu_q_lens[b] + i] = (int32_t)(c + i + 1); /* positions 0 .. c+i */
+        }
+    }
+    job_t J = {q, k_pool, v_pool, block_tables, seq_lens, row_req, row_len,
+               rows, M, H_q, H_kv, D, N, P, scale, dtype, out, 0, 0};
+    rc = run_job(&J, nthreads);
+    free(row_req);
+    free(row_len);
+    return rc;
+}
