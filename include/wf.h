@@ -1,0 +1,165 @@
+/*
+ * wf.h -- C ABI of libwf: attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * Three calls make up one attention step of an LLM serving engine that keeps
+ * its KV cache in fixed-size blocks:
+ *
+ *   wf_reshape_and_cache  write this step's new K/V rows into the block pool
+ *   wf_paged_decode       one query per sequence over its whole cached context
+ *   wf_paged_prefill      causal attention of new tokens over prefix + themselves
+ *
+ * Sources (page title, section):
+ *   weft, "Shapes and symbols": B, H_q, H_kv (H_q / H_kv = GQA group), D, N, P, T_total.
+ *   weft, "Cache layouts": per-layer paged view [N, P, H_kv, D]; write = scatter
+ *     via slot_mapping; read = gather by block_table; blocks handed out per request.
+ *   ember, "The core idea, in one picture": position p of a sequence lives in
+ *     block block_table[p // P] at offset p % P.
+ *   tiny-vllm-py, "KV Cache": the cache holds RoPE-rotated K and plain V; at
+ *     decode the new token attends to every earlier position and to itself; prefill
+ *     attention is causal ("Mistakes I made in Initial Implementation").
+ *
+ * Conventions for every call
+ *   - Every pointer argument is DEVICE memory owned by the caller, dense and
+ *     row-major as documented, 16-byte aligned.  The library allocates nothing,
+ *     keeps no per-call state, and never synchronises the stream (except
+ *     wf_device_status_fetch).  Calls are asynchronous and stream-ordered.
+ *   - q, k, v, pools and outputs all use the pool's dtype (float32 or bfloat16);
+ *     arithmetic is float32.  Outputs are rounded to nearest-even.
+ *   - Argument errors are returned synchronously, before anything is launched.
+ *   - Values that only the device can see (slots, block ids, sequence lengths)
+ *     are bounds-checked by the kernels: a bad one is skipped (never read or
+ *     written out of bounds) and a bit is OR-ed into *dev_status (a device
+ *     uint32_t; may be NULL to not record).  Read it with wf_device_status_fetch.
+ *   - Outputs never alias inputs.  K and V pools are separate buffers.
+ */
+#ifndef WF_H
+#define WF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum wf_status {
+    WF_OK = 0,
+    WF_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, H_q % H_kv != 0 */
+    WF_ERR_UNSUPPORTED = 2,  /* dtype / head_dim / group size this build does not handle     */
+    WF_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the *_workspace_size value */
+    WF_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed                  */
+} wf_status;
+
+typedef enum wf_dtype { WF_DTYPE_F32 = 0, WF_DTYPE_BF16 = 1 } wf_dtype;
+
+/* Bits the kernels OR into *dev_status. */
+#define WF_DEV_BAD_SLOT    0x1u  /* slot_mapping[t] >= N*P: token t not written              */
+#define WF_DEV_BAD_BLOCK   0x2u  /* block id outside [0, N): that block's rows were skipped  */
+#define WF_DEV_BAD_SEQLEN  0x4u  /* seq_lens[b] < 1, > max_seq_len, > M*P, or < q_len:
+                                    sequence b was skipped and its output left unwritten    */
+#define WF_DEV_TIMEOUT     0x8u  /* an internal pipeline wait gave up (should never happen) */
+
+/* One layer's pool geometry.  k_pool and v_pool are each [N, P, H_kv, D]. */
+typedef struct wf_pool_desc {
+    int32_t num_blocks;    /* N: blocks in the pool                       */
+    int32_t block_size;    /* P: tokens per block, 1 .. 1024              */
+    int32_t num_kv_heads;  /* H_kv                                        */
+    int32_t head_dim;      /* D: 64 or 128                                */
+    int32_t dtype;         /* wf_dtype of q, k, v, pools and outputs      */
+} wf_pool_desc;
+
+/*
+ * wf_reshape_and_cache -- scatter new K/V rows into the block pool.
+ * (weft, "Cache layouts": "write: scatter via slot_mapping")
+ *
+ *   k, v          [T, H_kv, D]   rows of this step's T new tokens
+ *   k_pool,v_pool [N, P, H_kv, D] updated in place
+ *   slot_mapping  [T] int64: token t goes to block slot/P, offset slot%P.
+ *                 A negative slot means "padding token": nothing is written.
+ *                 Two tokens with the same slot: one of them wins (unspecified).
+ *   num_tokens    T >= 0 (0 is a no-op)
+ * Pure byte copy: pool bytes equal the input bytes exactly.  Slots >= N*P are
+ * skipped and flagged WF_DEV_BAD_SLOT.
+ */
+wf_status wf_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               wf_pool_desc pool, uint32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Bytes of caller-allocated device workspace wf_paged_decode needs for a batch
+ * of at most B sequences of at most max_seq_len tokens.  Depends only on its
+ * arguments; 0 if they are invalid.
+ */
+size_t wf_paged_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_seq_len,
+                                      wf_pool_desc pool);
+
+/*
+ * wf_paged_decode -- one query token per sequence against its paged context.
+ * (ember, "The core idea"; tiny-vllm-py, "KV Cache": decode is not causal over
+ *  the cache and includes the just-written token)
+ *
+ *   out          [B, H_q, D]  out[b,g] = softmax_p(scale * q[b,g].K_p) V_p
+ *   q            [B, H_q, D]
+ *   k_pool, v_pool [N, P, H_kv, D] (already holding this step's new token)
+ *   block_tables [B, max_blocks_per_seq] int32, row-major.  Only the first
+ *                ceil(seq_lens[b] / P) entries of row b are read.
+ *   seq_lens     [B] int32: positions 0 .. seq_lens[b]-1 of sequence b are attended.
+ *                Must satisfy 1 <= seq_lens[b] <= max_seq_len <= max_blocks_per_seq*P.
+ *   num_q_heads  H_q; query head g reads KV head g / (H_q / H_kv).  H_q/H_kv <= 8.
+ *   scale        softmax scale (normally 1/sqrt(D))
+ *   workspace    device scratch of >= wf_paged_decode_workspace_size(B, H_q,
+ *                max_seq_len, pool) bytes, 16-byte aligned; contents need no
+ *                initialisation and are clobbered.  Calls that overlap in time
+ *                must not share a workspace.
+ * Launches a split-K kernel and, when any sequence spans more than one split, a
+ * combine kernel.  The split boundaries depend only on the pool geometry, so a
+ * sequence's output does not depend on the rest of the batch.
+ */
+wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                          int32_t num_q_heads, float scale, wf_pool_desc pool,
+                          void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                          cudaStream_t stream);
+
+/*
+ * wf_paged_prefill -- causal varlen attention of new tokens over the pool.
+ * (tiny-vllm-py, "KV Cache": prefill is causal; "Dense vs. Ragged batching":
+ *  requests are packed back to back with per-request offsets, no padding)
+ *
+ *   out        [T_total, H_q, D]
+ *   q          [T_total, H_q, D]: request b owns rows cu_q_lens[b] .. cu_q_lens[b+1]-1
+ *   cu_q_lens  [B+1] int32, cu_q_lens[0] = 0, non-decreasing, cu_q_lens[B] = T_total
+ *   seq_lens   [B] int32: tokens of request b in the pool INCLUDING its n_b new ones
+ *              (already written by wf_reshape_and_cache).  With c_b = seq_lens[b] - n_b,
+ *              query row i of request b attends to positions 0 .. c_b + i.
+ *   max_q_len  >= every n_b (sizes the launch)
+ * bfloat16 only; QK^T and PV run on the tensor cores (bf16 operands, fp32
+ * accumulation in tensor memory); the softmax weights are rounded to bf16 for PV.
+ */
+wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
+                           int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
+                           int32_t num_q_heads, float scale, wf_pool_desc pool,
+                           uint32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Wait for `stream`, copy *dev_status to *host_status and, if clear != 0, reset
+ * it to zero.  The only call that synchronises.
+ */
+wf_status wf_device_status_fetch(uint32_t* dev_status, uint32_t* host_status, int clear,
+                                 cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* wf_status_string(wf_status s);
+
+/* ABI version of this header (major * 100 + minor). */
+int wf_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WF_H */

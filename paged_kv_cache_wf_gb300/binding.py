@@ -1,0 +1,179 @@
+"""Thin Python binding of libwf's C ABI (include/wf.h).
+
+Argument marshalling only: every step of the attention path runs in the CUDA
+kernels of libwf.so.  Functions keep the C names and take torch CUDA tensors
+(or raw integers for pointers).  There is no fallback: if libwf.so is missing
+or cannot be loaded, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libwf.so")
+
+WF_OK, WF_ERR_INVALID_ARG, WF_ERR_UNSUPPORTED, WF_ERR_WORKSPACE, WF_ERR_CUDA = range(5)
+WF_DTYPE_F32, WF_DTYPE_BF16 = 0, 1
+WF_DEV_BAD_SLOT, WF_DEV_BAD_BLOCK, WF_DEV_BAD_SEQLEN, WF_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+# every entry point include/wf.h declares
+EXPORTS = (
+    "wf_reshape_and_cache",
+    "wf_paged_decode_workspace_size",
+    "wf_paged_decode",
+    "wf_paged_prefill",
+    "wf_device_status_fetch",
+    "wf_status_string",
+    "wf_abi_version",
+)
+
+
+class wf_pool_desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class WfError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn}: {status_string(code)} (status {code})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libwf.so (built by paged_kv_cache_wf_gb300.build); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libwf.so not found at {path}: run paged_kv_cache_wf_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        lib.wf_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, wf_pool_desc, vp, vp]
+        lib.wf_reshape_and_cache.restype = ctypes.c_int
+        lib.wf_paged_decode_workspace_size.argtypes = [i32, i32, i32, wf_pool_desc]
+        lib.wf_paged_decode_workspace_size.restype = sz
+        lib.wf_paged_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, f32, wf_pool_desc,
+                                        vp, sz, vp, vp]
+        lib.wf_paged_decode.restype = ctypes.c_int
+        lib.wf_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, f32,
+                                         wf_pool_desc, vp, vp]
+        lib.wf_paged_prefill.restype = ctypes.c_int
+        lib.wf_device_status_fetch.argtypes = [vp, vp, ctypes.c_int, vp]
+        lib.wf_device_status_fetch.restype = ctypes.c_int
+        lib.wf_status_string.argtypes = [ctypes.c_int]
+        lib.wf_status_string.restype = ctypes.c_char_p
+        lib.wf_abi_version.argtypes = []
+        lib.wf_abi_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().wf_status_string(code).decode()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int):
+    if rc != WF_OK:
+        raise WfError(fn, rc)
+
+
+def pool_desc(k_pool) -> wf_pool_desc:
+    """Pool geometry from a [N, P, H_kv, D] float32 / bfloat16 tensor."""
+    import torch
+    N, P, H_kv, D = k_pool.shape
+    if k_pool.dtype == torch.float32:
+        dt = WF_DTYPE_F32
+    elif k_pool.dtype == torch.bfloat16:
+        dt = WF_DTYPE_BF16
+    else:
+        raise TypeError(f"unsupported pool dtype {k_pool.dtype}")
+    return wf_pool_desc(N, P, H_kv, D, dt)
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not isinstance(t, int) and not t.is_contiguous():
+            raise ValueError("libwf takes dense row-major tensors")
+
+
+# ---------------------------------------------------------------------------
+# the C entry points, torch-tensor flavoured
+# ---------------------------------------------------------------------------
+def wf_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, dev_status=None, stream=None):
+    """Scatter k, v [T, H_kv, D] into k_pool, v_pool [N, P, H_kv, D] via slot_mapping [T] int64."""
+    _contig(k, v, k_pool, v_pool, slot_mapping)
+    lib = load()
+    rc = lib.wf_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping),
+                                  int(slot_mapping.shape[0]), pool_desc(k_pool), _ptr(dev_status),
+                                  _stream(stream))
+    _check("wf_reshape_and_cache", rc)
+
+
+def wf_paged_decode_workspace_size(B: int, num_q_heads: int, max_seq_len: int, desc: wf_pool_desc) -> int:
+    return int(load().wf_paged_decode_workspace_size(B, num_q_heads, max_seq_len, desc))
+
+
+def wf_paged_decode(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len: int, scale: float,
+                    workspace, dev_status=None, stream=None):
+    """out, q [B, H_q, D]; block_tables [B, M] int32; seq_lens [B] int32; workspace uint8 tensor."""
+    _contig(out, q, k_pool, v_pool, block_tables, seq_lens)
+    lib = load()
+    B, H_q, _ = q.shape
+    rc = lib.wf_paged_decode(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                             int(block_tables.shape[1]), _ptr(seq_lens), int(B), int(max_seq_len),
+                             int(H_q), float(scale), pool_desc(k_pool), _ptr(workspace),
+                             int(workspace.numel() * workspace.element_size()), _ptr(dev_status),
+                             _stream(stream))
+    _check("wf_paged_decode", rc)
+
+
+def wf_paged_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens, max_q_len: int,
+                     max_seq_len: int, scale: float, dev_status=None, stream=None):
+    """out, q [T_total, H_q, D] bf16; cu_q_lens [B+1] int32; seq_lens include the new tokens."""
+    _contig(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens)
+    lib = load()
+    T, H_q, _ = q.shape
+    B = int(seq_lens.shape[0])
+    rc = lib.wf_paged_prefill(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                              int(block_tables.shape[1]), _ptr(seq_lens), _ptr(cu_q_lens), B, int(T),
+                              int(max_q_len), int(max_seq_len), int(H_q), float(scale),
+                              pool_desc(k_pool), _ptr(dev_status), _stream(stream))
+    _check("wf_paged_prefill", rc)
+
+
+def wf_device_status_fetch(dev_status, clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return (optionally clearing) the device status word."""
+    lib = load()
+    host = ctypes.c_uint32(0)
+    rc = lib.wf_device_status_fetch(_ptr(dev_status), ctypes.addressof(host), int(bool(clear)),
+                                    _stream(stream))
+    _check("wf_device_status_fetch", rc)
+    return int(host.value)

@@ -1,0 +1,171 @@
+// wf_api.cu -- the extern "C" boundary of libwf: argument validation (before any
+// launch), status mapping, and dispatch to the kernels' launchers.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <unordered_map>
+
+#include "wf_internal.h"
+
+namespace wf {
+
+int num_sms() {
+    static std::mutex mu;
+    static std::unordered_map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+    cache[dev] = n;
+    return n;
+}
+
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> done;  // (device, kernel) -> bytes granted
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t key = (reinterpret_cast<uint64_t>(kernel) << 8) ^ (uint64_t)dev;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    if (bytes > 48 * 1024) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (err != cudaSuccess) return err;
+    }
+    done[key] = bytes;
+    return cudaSuccess;
+}
+
+}  // namespace wf
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+wf_status check_pool(const wf_pool_desc& pool) {
+    if (pool.num_blocks < 1 || pool.block_size < 1 || pool.block_size > 1024 ||
+        pool.num_kv_heads < 1)
+        return WF_ERR_INVALID_ARG;
+    if (pool.dtype != WF_DTYPE_F32 && pool.dtype != WF_DTYPE_BF16) return WF_ERR_UNSUPPORTED;
+    if (pool.head_dim != 64 && pool.head_dim != 128) return WF_ERR_UNSUPPORTED;
+    const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
+    if (slots > (int64_t)INT32_MAX * 64) return WF_ERR_INVALID_ARG;
+    return WF_OK;
+}
+
+wf_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return WF_OK;
+    if (e == cudaErrorNotSupported) return WF_ERR_UNSUPPORTED;
+    return WF_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wf_abi_version(void) { return 100; }
+
+const char* wf_status_string(wf_status s) {
+    switch (s) {
+        case WF_OK: return "ok";
+        case WF_ERR_INVALID_ARG: return "invalid argument";
+        case WF_ERR_UNSUPPORTED: return "unsupported configuration";
+        case WF_ERR_WORKSPACE: return "workspace missing or too small";
+        case WF_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+wf_status wf_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               wf_pool_desc pool, uint32_t* dev_status, cudaStream_t stream) {
+    wf_status s = check_pool(pool);
+    if (s != WF_OK) return s;
+    if (num_tokens < 0) return WF_ERR_INVALID_ARG;
+    if (num_tokens == 0) return WF_OK;
+    if (!k || !v || !k_pool || !v_pool || !slot_mapping) return WF_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return WF_ERR_INVALID_ARG;
+    return from_cuda(wf::launch_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, num_tokens,
+                                                  pool, dev_status, stream));
+}
+
+size_t wf_paged_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_seq_len,
+                                      wf_pool_desc pool) {
+    if (check_pool(pool) != WF_OK || num_q_heads < 1) return 0;
+    return wf::decode_workspace_bytes(B, num_q_heads, max_seq_len, pool);
+}
+
+wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                          int32_t num_q_heads, float scale, wf_pool_desc pool,
+                          void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                          cudaStream_t stream) {
+    wf_status s = check_pool(pool);
+    if (s != WF_OK) return s;
+    if (B < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 1) return WF_ERR_INVALID_ARG;
+    if (num_q_heads % pool.num_kv_heads != 0) return WF_ERR_INVALID_ARG;
+    if (num_q_heads / pool.num_kv_heads > 8) return WF_ERR_UNSUPPORTED;
+    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool.block_size) return WF_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return WF_ERR_INVALID_ARG;
+    if (B == 0) return WF_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens) return WF_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return WF_ERR_INVALID_ARG;
+    const size_t need = wf::decode_workspace_bytes(B, num_q_heads, max_seq_len, pool);
+    if (need == 0) return WF_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return WF_ERR_WORKSPACE;
+    return from_cuda(wf::launch_paged_decode(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                                             seq_lens, B, max_seq_len, num_q_heads, scale, pool,
+                                             workspace, dev_status, stream));
+}
+
+wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
+                           int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
+                           int32_t num_q_heads, float scale, wf_pool_desc pool,
+                           uint32_t* dev_status, cudaStream_t stream) {
+    wf_status s = check_pool(pool);
+    if (s != WF_OK) return s;
+    if (pool.dtype != WF_DTYPE_BF16) return WF_ERR_UNSUPPORTED;
+    if (B < 0 || total_q < 0 || max_q_len < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 ||
+        max_seq_len < 0)
+        return WF_ERR_INVALID_ARG;
+    if (num_q_heads % pool.num_kv_heads != 0) return WF_ERR_INVALID_ARG;
+    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool.block_size) return WF_ERR_INVALID_ARG;
+    if (max_q_len > max_seq_len) return WF_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return WF_ERR_INVALID_ARG;
+    if (B == 0 || total_q == 0 || max_q_len == 0) return WF_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !cu_q_lens)
+        return WF_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u))
+        return WF_ERR_INVALID_ARG;
+    return from_cuda(wf::launch_paged_prefill(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                                              seq_lens, cu_q_lens, B, total_q, max_q_len, max_seq_len,
+                                              num_q_heads, scale, pool, dev_status, stream));
+}
+
+wf_status wf_device_status_fetch(uint32_t* dev_status, uint32_t* host_status, int clear,
+                                 cudaStream_t stream) {
+    if (!dev_status || !host_status) return WF_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(host_status, dev_status, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && clear) {
+        e = cudaMemsetAsync(dev_status, 0, sizeof(uint32_t), stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    return from_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// wf_internal.h -- host-side declarations shared by the libwf translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/wf.h"
+#include "wf_device.cuh"
+
+namespace wf {
+
+inline int dtype_bytes(int32_t dtype) { return dtype == WF_DTYPE_F32 ? 4 : 2; }
+
+// SM count of the current device (cached per device).
+int num_sms();
+
+// Opt a kernel into `bytes` of dynamic shared memory (idempotent, cached).
+cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                                     const int64_t* slot_mapping, int32_t num_tokens,
+                                     const wf_pool_desc& pool, uint32_t* dev_status,
+                                     cudaStream_t stream);
+
+// ---- decode -----------------------------------------------------------------
+// Positions are cut into fixed spans ("splits") that depend only on the pool
+// geometry; each split is one CTA's work and leaves a partial (m, l, o).
+struct DecodeGeometry {
+    int split_span;   // positions per split (multiple of the tile)
+    int tile;         // positions per pipeline stage
+    int stages;       // pipeline depth
+    int smem_bytes;   // dynamic shared memory per CTA
+    int consumer_warps;
+    int heads_per_warp;
+    int gmax;         // padded GQA group the kernel instance handles
+};
+
+bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeometry* g);
+size_t decode_workspace_bytes(int32_t B, int32_t num_q_heads, int32_t max_seq_len,
+                              const wf_pool_desc& pool);
+
+cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                                int32_t num_q_heads, float scale, const wf_pool_desc& pool,
+                                void* workspace, uint32_t* dev_status, cudaStream_t stream);
+
+// ---- prefill ----------------------------------------------------------------
+cudaError_t launch_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
+                                 int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
+                                 int32_t num_q_heads, float scale, const wf_pool_desc& pool,
+                                 uint32_t* dev_status, cudaStream_t stream);
+
+}  // namespace wf

@@ -37,9 +37,8 @@ BF16 = "bf16"
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (round-to-nearest-even), as uint16 bit patterns."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounding_bias = ((u >> 16) & 1) + 0x7FFF
-    out = ((u + rounding_bias) >> 16).astype(np.uint16)
+    u = x.view(np.uint32)
+    out = ((u + (((u >> 16) & 1) + np.uint32(0x7FFF))) >> 16).astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
         out[nan] = 0x7FC0
@@ -396,6 +395,55 @@ def mixed_step(seed: int = 0, n_prefill: int = 8, n_decode: int = 120) -> Tuple[
     dc = Layout(both.geom, seq[n_prefill:], ql[n_prefill:],
                 both.block_tables[n_prefill:].copy(), both.spare_block)
     return pf, dc
+
+
+# ---------------------------------------------------------------------------
+# device-side values for the large workloads (host RNG would take minutes)
+# ---------------------------------------------------------------------------
+def live_slot_mask(layouts) -> np.ndarray:
+    """bool [N*P]: slots that hold a cached prefix position of some sequence."""
+    layouts = layouts if isinstance(layouts, (list, tuple)) else [layouts]
+    g = layouts[0].geom
+    live = np.zeros(g.N * g.P, dtype=bool)
+    for lay in layouts:
+        live[lay.prefix_slots()] = True
+    return live
+
+
+def device_pools(layouts, seed: int, device="cuda"):
+    """K and V pools on the device: N(0,1)*scale bf16/f32 draws from a seeded torch
+    generator in every slot that holds a cached prefix position, NaN elsewhere
+    (this step's new slots included: the step's scatter fills them)."""
+    import torch
+    layouts = layouts if isinstance(layouts, (list, tuple)) else [layouts]
+    g = layouts[0].geom
+    tdt = torch.float32 if g.dtype == F32 else torch.bfloat16
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    dead = torch.from_numpy(~live_slot_mask(layouts)).to(device)
+    pools = []
+    for _ in range(2):
+        pool = torch.empty((g.N * g.P, g.H_kv, g.D), dtype=tdt, device=device)
+        pool.normal_(0.0, g.value_scale, generator=gen)
+        pool[dead] = float("nan")
+        pools.append(pool.view(g.N, g.P, g.H_kv, g.D))
+    return pools[0], pools[1]
+
+
+def device_step_values(layout: Layout, seed: int, device="cuda"):
+    """q [T_total, H_q, D], k_new, v_new [T_total, H_kv, D] on the device (seeded torch draws)."""
+    import torch
+    g = layout.geom
+    tdt = torch.float32 if g.dtype == F32 else torch.bfloat16
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    T = layout.T_total
+    out = []
+    for shape in ((T, g.H_q, g.D), (T, g.H_kv, g.D), (T, g.H_kv, g.D)):
+        t = torch.empty(shape, dtype=tdt, device=device)
+        t.normal_(0.0, g.value_scale, generator=gen)
+        out.append(t)
+    return tuple(out)
 
 
 WORKLOADS = {

@@ -1,0 +1,131 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports every
+entry point include/wf.h declares, and rejects bad arguments before launching
+anything (these calls return before any CUDA call, so no GPU is needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_cache_wf_gb300 import binding as wf
+from paged_kv_cache_wf_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # 16-byte aligned non-null address; never dereferenced by these calls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return wf.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(wf_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.check_output(["nm", "-D", "--defined-only", build.LIB], text=True)
+    exported = set(re.findall(r"\bT (wf_[a-z0-9_]+)", out))
+    declared = _declared()
+    assert declared, "no declarations found"
+    assert declared <= exported, declared - exported
+    assert declared == set(wf.EXPORTS)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.wf_abi_version() == 100
+    for code in range(5):
+        assert wf.status_string(code)
+
+
+def _desc(N=10, P=16, H=2, D=64, dt=wf.WF_DTYPE_BF16):
+    return wf.wf_pool_desc(N, P, H, D, dt)
+
+
+def test_scatter_argument_checks(lib):
+    d = _desc()
+    f = lib.wf_reshape_and_cache
+    assert f(None, None, None, None, None, 0, d, None, None) == wf.WF_OK  # T = 0: no-op
+    assert f(None, None, None, None, None, 3, d, None, None) == wf.WF_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, d, None, None) == wf.WF_ERR_INVALID_ARG
+    assert f(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 3, d, None, None) == wf.WF_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, _desc(D=96), None, None) == wf.WF_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, _desc(dt=7), None, None) == wf.WF_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, _desc(P=0), None, None) == wf.WF_ERR_INVALID_ARG
+
+
+def test_decode_workspace_size(lib):
+    d = _desc(N=100, P=16, H=8, D=128)
+    a = wf.wf_paged_decode_workspace_size(231, 32, 8704, d)
+    b = wf.wf_paged_decode_workspace_size(231, 32, 128, d)
+    assert a > b > 0
+    assert wf.wf_paged_decode_workspace_size(4, 31, 100, d) == 0      # H_q % H_kv != 0
+    assert wf.wf_paged_decode_workspace_size(4, 32, 0, d) == 0
+
+
+def test_decode_argument_checks(lib):
+    d = _desc(N=10, P=16, H=2, D=64)
+    f = lib.wf_paged_decode
+    ws = wf.wf_paged_decode_workspace_size(4, 8, 64, d)
+    ok = dict(out=FAKE, q=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, M=4, sl=FAKE, B=4, msl=64, Hq=8, scale=0.1,
+              d=d, ws=FAKE, wsb=ws)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["out"], a["q"], a["kp"], a["vp"], a["bt"], a["M"], a["sl"], a["B"], a["msl"], a["Hq"],
+                 a["scale"], a["d"], a["ws"], a["wsb"], None, None)
+
+    assert call(B=0) == wf.WF_OK
+    assert call(Hq=7) == wf.WF_ERR_INVALID_ARG                 # H_q % H_kv != 0
+    assert call(Hq=18, d=_desc(N=10, P=16, H=2, D=64)) == wf.WF_ERR_UNSUPPORTED  # G = 9 > 8
+    assert call(msl=65) == wf.WF_ERR_INVALID_ARG               # max_seq_len > M * P
+    assert call(scale=float("inf")) == wf.WF_ERR_INVALID_ARG
+    assert call(q=None) == wf.WF_ERR_INVALID_ARG
+    assert call(out=FAKE + 8) == wf.WF_ERR_INVALID_ARG         # misaligned
+    assert call(wsb=ws - 1) == wf.WF_ERR_WORKSPACE
+    assert call(ws=None) == wf.WF_ERR_WORKSPACE
+    assert call(d=_desc(D=80)) == wf.WF_ERR_UNSUPPORTED
+
+
+def test_prefill_argument_checks(lib):
+    d = _desc(N=10, P=16, H=2, D=128)
+    f = lib.wf_paged_prefill
+
+    def call(d=d, B=2, T=10, mq=8, msl=40, Hq=8, q=FAKE, cu=FAKE):
+        return f(FAKE, q, FAKE, FAKE, FAKE, 4, FAKE, cu, B, T, mq, msl, Hq, 0.1, d, None, None)
+
+    assert call(B=0) == wf.WF_OK
+    assert call(T=0) == wf.WF_OK
+    assert call(d=_desc(dt=wf.WF_DTYPE_F32, D=128)) == wf.WF_ERR_UNSUPPORTED   # bf16 only
+    assert call(Hq=9) == wf.WF_ERR_INVALID_ARG
+    assert call(msl=65) == wf.WF_ERR_INVALID_ARG
+    assert call(mq=50) == wf.WF_ERR_INVALID_ARG                # max_q_len > max_seq_len
+    assert call(cu=None) == wf.WF_ERR_INVALID_ARG
+    assert call(q=FAKE + 2) == wf.WF_ERR_INVALID_ARG
+
+
+def test_status_fetch_rejects_null(lib):
+    assert lib.wf_device_status_fetch(None, None, 1, None) == wf.WF_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        wf.load.__wrapped__(str(tmp_path / "nope.so")) if hasattr(wf.load, "__wrapped__") else \
+            _load_fresh(str(tmp_path / "nope.so"))
+
+
+def _load_fresh(path):
+    saved = wf._lib
+    wf._lib = None
+    try:
+        return wf.load(path)
+    finally:
+        wf._lib = saved
