@@ -1,0 +1,522 @@
+"""Benchmark of the paged-KV attention hot path on one GB300 (or N replicas).
+
+A step is one decode step of a 32-layer Llama-3-8B-shaped model's attention:
+for every layer, wf_reshape_and_cache writes the B new tokens' K/V into that
+layer's pool and wf_paged_decode attends each sequence over its whole paged
+context (H_q=32, H_kv=8, D=128, P=16, bf16, B=231 by default).  Every layer has
+its own pool (~2.2 GB with the allocator's headroom), so each launch streams
+from HBM, never from the 129 MB L2.
+
+Printed (rank 0, one JSON line): sequences*layers/s, the decode call's roofline
+against the measured HBM copy bandwidth, an end-to-end figure through host
+buffers, the oracle's CPU time on a bounded sample, launch count and clocks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--batch 118|231]
+                    [--workload llama8b|mixed] [--impl wf|reference]
+
+Under torchrun each rank runs its own replica on its own GPU (no data-path
+collective; sequences are independent) and the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_wf_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: sequences·layers/s and achieved HBM GB/s (% of ~8 TB/s)"
+UNIT = "seq·layers/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_wf_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if taken on this exact source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("workload") != workload:
+        return None
+    if rec.get("source_sha") != source_digest(rec.get("sources", [])):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"wf_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; no block padding)
+# ---------------------------------------------------------------------------
+def decode_bytes(lay) -> int:
+    g = lay.geom
+    e = W.elt_size(g.dtype)
+    kv = int(2 * lay.seq_lens.astype(np.int64).sum() * g.H_kv * g.D * e)
+    qo = 2 * lay.B * g.H_q * g.D * e
+    tables = int(sum(-(-int(s) // g.P) for s in lay.seq_lens) * 4) + 4 * lay.B
+    return kv + qo + tables
+
+
+def scatter_bytes(T: int, g) -> int:
+    return 2 * 2 * T * g.H_kv * g.D * W.elt_size(g.dtype) + 8 * T
+
+
+def prefill_flops(lay) -> float:
+    g = lay.geom
+    tot = 0
+    for b in range(lay.B):
+        c, n = int(lay.prefix_lens[b]), int(lay.q_lens[b])
+        tot += n * c + n * (n + 1) // 2          # sum_{i<n} (c + i + 1)
+    return 4.0 * g.H_q * g.D * tot
+
+
+# ---------------------------------------------------------------------------
+# the wf arm
+# ---------------------------------------------------------------------------
+class DecodeWorkload:
+    """L layers of (scatter of B new tokens, paged decode), one pool per layer."""
+
+    def __init__(self, lay, layers: int, seed: int):
+        import torch
+        from paged_kv_cache_wf_gb300 import binding as wf
+        self.torch, self.wf = torch, wf
+        self.lib = wf.load()
+        self.lay = lay
+        g = lay.geom
+        self.L = layers
+        self.pools = [W.device_pools(lay, seed=seed + 17 * l) for l in range(layers)]
+        self.vals = [W.device_step_values(lay, seed=seed + 17 * l + 5) for l in range(layers)]
+        self.outs = [torch.empty_like(v[0]) for v in self.vals]
+        self.bt = torch.from_numpy(lay.block_tables).cuda()
+        self.sl = torch.from_numpy(lay.seq_lens).cuda()
+        self.slots = torch.from_numpy(lay.new_slots()).cuda()
+        self.desc = wf.pool_desc(self.pools[0][0])
+        self.max_seq_len = lay.max_seq_len
+        self.ws_bytes = wf.wf_paged_decode_workspace_size(lay.B, g.H_q, self.max_seq_len, self.desc)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.scale = 1.0 / math.sqrt(g.D)
+        self.stream = torch.cuda.current_stream()
+        self.sp = self.stream.cuda_stream
+        self.launches_per_layer = 2 + (1 if -(-self.max_seq_len // self.split_span()) > 1 else 0)
+
+    def split_span(self) -> int:
+        return 128
+
+    def _scatter(self, l, k=None, v=None, slots=None):
+        kp, vp = self.pools[l]
+        kk = k if k is not None else self.vals[l][1]
+        vv = v if v is not None else self.vals[l][2]
+        ss = slots if slots is not None else self.slots
+        rc = self.lib.wf_reshape_and_cache(kk.data_ptr(), vv.data_ptr(), kp.data_ptr(), vp.data_ptr(),
+                                           ss.data_ptr(), int(ss.shape[0]), self.desc, self.status.data_ptr(),
+                                           self.sp)
+        assert rc == 0, rc
+
+    def _decode(self, l, q=None, bt=None, sl=None, out=None):
+        kp, vp = self.pools[l]
+        qq = q if q is not None else self.vals[l][0]
+        oo = out if out is not None else self.outs[l]
+        bt = bt if bt is not None else self.bt
+        sl = sl if sl is not None else self.sl
+        rc = self.lib.wf_paged_decode(oo.data_ptr(), qq.data_ptr(), kp.data_ptr(), vp.data_ptr(), bt.data_ptr(),
+                                      int(bt.shape[1]), sl.data_ptr(), self.lay.B, self.max_seq_len,
+                                      self.lay.geom.H_q, self.scale, self.desc, self.ws.data_ptr(), self.ws_bytes,
+                                      self.status.data_ptr(), self.sp)
+        assert rc == 0, rc
+
+    def step(self, events=None):
+        for l in range(self.L):
+            self._scatter(l)
+            if events is not None:
+                e0, e1 = events.pop()
+                e0.record(self.stream)
+                self._decode(l)
+                e1.record(self.stream)
+                self._ev_done.append((e0, e1))
+            else:
+                self._decode(l)
+
+    def timed(self, steps: int, per_launch: bool = True):
+        torch = self.torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps * self.L)] if per_launch else None
+        self._ev_done = []
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(self.stream)
+        for _ in range(steps):
+            self.step(ev)
+        end.record(self.stream)
+        end.synchronize()
+        total_ms = start.elapsed_time(end)
+        launch_ms = [a.elapsed_time(b) for a, b in self._ev_done] if per_launch else []
+        return total_ms, launch_ms
+
+
+class E2EDecode:
+    """The same step through host buffers: per layer, q / k_new / v_new come from
+    pinned host memory and the attention output goes back to pinned host memory;
+    block tables, lengths and slots are uploaded once per step."""
+
+    def __init__(self, wl: DecodeWorkload):
+        torch = wl.torch
+        self.wl = wl
+        self.h_vals = [tuple(t.cpu().pin_memory() for t in v) for v in wl.vals]
+        self.h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in wl.outs]
+        self.h_bt = wl.bt.cpu().pin_memory()
+        self.h_sl = wl.sl.cpu().pin_memory()
+        self.h_slots = wl.slots.cpu().pin_memory()
+        self.d_vals = [torch.empty_like(t) for t in wl.vals[0]]
+        self.d_bt, self.d_sl, self.d_slots = (torch.empty_like(wl.bt), torch.empty_like(wl.sl),
+                                              torch.empty_like(wl.slots))
+        nb = lambda t: t.numel() * t.element_size()
+        self.h2d = (sum(nb(t) for v in self.h_vals for t in v) + nb(self.h_bt) + nb(self.h_sl)
+                    + nb(self.h_slots))
+        self.d2h = sum(nb(t) for t in self.h_out)
+
+    def step(self):
+        wl = self.wl
+        self.d_bt.copy_(self.h_bt, non_blocking=True)
+        self.d_sl.copy_(self.h_sl, non_blocking=True)
+        self.d_slots.copy_(self.h_slots, non_blocking=True)
+        for l in range(wl.L):
+            q, k, v = self.d_vals
+            hq, hk, hv = self.h_vals[l]
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            wl._scatter(l, k, v, self.d_slots)
+            wl._decode(l, q, self.d_bt, self.d_sl, wl.outs[l])
+            self.h_out[l].copy_(wl.outs[l], non_blocking=True)
+
+    def timed(self, steps: int):
+        torch = self.wl.torch
+        s = self.wl.stream
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(s)
+        for _ in range(steps):
+            self.step()
+        end.record(s)
+        end.synchronize()
+        return start.elapsed_time(end)
+
+
+# ---------------------------------------------------------------------------
+# the oracle (reference arm and CPU baseline)
+# ---------------------------------------------------------------------------
+def oracle_sample_inputs(lay, seed: int, wl=None):
+    """Host inputs of one layer for the oracle: the blocks the batch uses and this
+    step's new rows.  Taken from the device pools when a wf workload exists (the
+    values the GPU sees), else drawn on the host."""
+    g = lay.geom
+    if wl is not None:
+        torch = wl.torch
+        kp, vp = wl.pools[0]
+        q, kn, vn = wl.vals[0]
+        nb = [-(-int(s) // g.P) for s in lay.seq_lens]
+        used = np.unique(np.concatenate([lay.block_tables[b, :n] for b, n in enumerate(nb)]))
+        remap = np.zeros(g.N, np.int32)
+        remap[used] = np.arange(used.shape[0], dtype=np.int32)
+        idx = torch.from_numpy(used.astype(np.int64)).cuda()
+        bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+        # pool contents before this step's write: the new slots are NaN in both
+        hk, hv = bits(kp.index_select(0, idx)), bits(vp.index_select(0, idx))
+        bt = np.zeros_like(lay.block_tables)
+        for b, n in enumerate(nb):
+            bt[b, :n] = remap[lay.block_tables[b, :n]]
+        sub = W.Layout(W.Geometry(g.H_q, g.H_kv, g.D, g.P, used.shape[0], g.dtype), lay.seq_lens, lay.q_lens,
+                       bt, 0)
+        return sub, hk, hv, bits(q), bits(kn), bits(vn)
+    rng = np.random.default_rng(seed)
+    vals = W.draw_layer_values(lay, rng)
+    import oracle
+    hk, hv = W.empty_pool(g), W.empty_pool(g)
+    oracle.reshape_and_cache(vals.k_prefix, vals.v_prefix, hk, hv, lay.prefix_slots(), g.dtype)
+    return lay, hk, hv, vals.q, vals.k_new, vals.v_new
+
+
+def oracle_time(sub, hk, hv, q, kn, vn, min_seconds: float, max_reps: int):
+    """Time scatter + decode of one layer of the batch in the oracle, repeated."""
+    import oracle
+    g = sub.geom
+    scale = 1.0 / math.sqrt(g.D)
+    slots = sub.new_slots()
+    threads = os.cpu_count() or 1
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        kp, vp = hk.copy(), hv.copy()
+        oracle.reshape_and_cache(kn, vn, kp, vp, slots, g.dtype)
+        oracle.paged_decode(q, kp, vp, sub.block_tables, sub.seq_lens, scale, g.dtype, threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            return reps, el, threads
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def make_layout(args):
+    if args.workload == "llama8b":
+        return W.llama8b_decode(args.batch, seed=0), f"llama8b_decode_B{args.batch}"
+    if args.workload == "gpt2":
+        return W.gpt2_decode(0), "gpt2_decode_B32"
+    if args.workload == "llama1b":
+        return W.llama1b_decode(0), "llama1b_decode_B64"
+    raise SystemExit(f"unknown workload {args.workload}")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    lay, wname = make_layout(args)
+    g = lay.geom
+    L = g.L
+    sub, hk, hv, q, kn, vn = oracle_sample_inputs(lay, seed=0)
+    for _ in range(max(0, args.warmup)):
+        oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1)
+    times = []
+    for _ in range(args.steps):
+        reps, el, threads = oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1)
+        times.append(el)
+    per_layer = sum(times) / len(times)
+    value = lay.B / per_layer
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * L * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wname, "B": lay.B, "layers": L, "H_q": g.H_q, "H_kv": g.H_kv, "D": g.D,
+                   "P": g.P, "kv_dtype": g.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"each timed step = one layer of the {wname} batch (all {lay.B} sequences, "
+                                   f"scatter + decode) in the fp64 oracle; ms_per_step scales it to {L} layers"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=231, choices=[118, 231])
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "gpt2", "llama1b"])
+    ap.add_argument("--impl", default="wf", choices=["wf", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run this many layers instead of the model's (recorded in config)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    from paged_kv_cache_wf_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if pg is not None:
+        pg.barrier()
+
+    lay, wname = make_layout(args)
+    g = lay.geom
+    L = args.layers if args.layers > 0 else g.L
+    wl = DecodeWorkload(lay, L, seed=1000 + 7919 * rank)
+    # oracle inputs are copied before any kernel of ours has touched the pools
+    oracle_in = None
+    if rank == 0 and not args.no_cpu_baseline:
+        oracle_in = oracle_sample_inputs(lay, 0, wl)
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    if wl.wf.wf_device_status_fetch(wl.status) != 0:
+        raise SystemExit("device status flagged an error during warm-up")
+
+    # ---- timed region ---------------------------------------------------------
+    clocks = ClockSampler(torch.cuda.current_device())
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    total_ms, launch_ms = wl.timed(args.steps, per_launch=True)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if pg is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * lay.B * L / (ms_per_step / 1e3)
+
+    # ---- roofline of the decode call (split + combine kernels) -------------------
+    peaks, peak_src = load_peaks()
+    dbytes = decode_bytes(lay)
+    avg_launch_s = (sum(launch_ms) / len(launch_ms)) / 1e3
+    achieved = dbytes / avg_launch_s / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    step_bytes = L * (dbytes + scatter_bytes(lay.B, g))
+    traffic = recorded_traffic("paged_decode", wname)
+
+    # ---- end to end through host buffers --------------------------------------------
+    e2e = None
+    if not args.no_e2e:
+        ee = E2EDecode(wl)
+        for _ in range(3):
+            ee.step()
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+        e_ms = ee.timed(args.steps) / args.steps
+        if pg is not None:
+            t = torch.tensor([e_ms], device="cuda")
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * lay.B * L / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": ee.h2d, "d2h_bytes_per_step": ee.d2h}
+        del ee
+
+    # ---- oracle on the host cores (rank 0 only) ------------------------------------------
+    cpu = None
+    if oracle_in is not None:
+        sub, hk, hv, q, kn, vn = oracle_in
+        oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1)  # warm
+        reps, el, threads = oracle_time(sub, hk, hv, q, kn, vn, args.cpu_seconds, 1000)
+        cpu = {"value": lay.B * reps / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"layer 0 of the {wname} batch (all {lay.B} sequences: scatter + decode), "
+                         f"repeated {reps}x in {el:.1f} s with {threads} threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wname, "B": lay.B, "layers": L, "model_layers": g.L, "H_q": g.H_q,
+                       "H_kv": g.H_kv, "D": g.D, "P": g.P, "N_blocks_per_layer": g.N, "kv_dtype": g.dtype,
+                       "context_tokens": int(lay.seq_lens.sum()), "max_seq_len": lay.max_seq_len,
+                       "l2": "inputs larger than L2: each layer's pools are %.2f GB, read once per step"
+                             % (2 * g.N * g.P * g.H_kv * g.D * 2 / 1e9),
+                       "parallelism": f"replicas{world}"},
+            "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
+            "pct_of_nominal_8tbs_step": 100.0 * step_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+            "roofline": {"kernel": "wf_paged_decode (split + combine)", "bound": "hbm", "achieved": achieved,
+                         "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_source": peak_src,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": dbytes,
+                         "avg_launch_us": avg_launch_s * 1e6,
+                         "pct_of_nominal_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * L * wl.launches_per_layer,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
