@@ -147,6 +147,43 @@ wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const v
                            uint32_t* dev_status, cudaStream_t stream);
 
 /*
+ * Size of the fixed device array wf_paged_decode_static_scratch uses as its
+ * workspace (32 MiB).  Every GPU that loads libwf holds it until the process exits.
+ */
+#define WF_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * wf_paged_decode_static_scratch -- wf_paged_decode for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is a library
+ * convenience, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc when they run attention: an allocator or
+ * memory manager that must not re-enter itself, a plugin whose host framework
+ * owns every device allocation, or a runtime that forbids allocation after
+ * start-up to keep its memory use fixed.  This call takes the same arguments as
+ * wf_paged_decode except the workspace: it uses a file-scope device array of
+ * WF_STATIC_SCRATCH_BYTES instead, and it allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library call).
+ *
+ *   - Returns WF_ERR_WORKSPACE, before launching anything, when the batch needs
+ *     more than WF_STATIC_SCRATCH_BYTES (compare
+ *     wf_paged_decode_workspace_size(B, num_q_heads, max_seq_len, pool)).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls that overlap in
+ *     time on the same device, e.g. on two streams, race on it and give wrong
+ *     results: serialise them.
+ */
+wf_status wf_paged_decode_static_scratch(void* out, const void* q, const void* k_pool,
+                                         const void* v_pool, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                         int32_t B, int32_t max_seq_len, int32_t num_q_heads,
+                                         float scale, wf_pool_desc pool, uint32_t* dev_status,
+                                         cudaStream_t stream);
+
+/*
  * Wait for `stream`, copy *dev_status to *host_status and, if clear != 0, reset
  * it to zero.  The only call that synchronises.
  */

@@ -24,6 +24,7 @@ EXPORTS = (
     "wf_paged_decode_workspace_size",
     "wf_paged_decode",
     "wf_paged_prefill",
+    "wf_paged_decode_static_scratch",
     "wf_device_status_fetch",
     "wf_status_string",
     "wf_abi_version",
@@ -66,6 +67,9 @@ def load(path: str = LIB_PATH):
         lib.wf_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, f32,
                                          wf_pool_desc, vp, vp]
         lib.wf_paged_prefill.restype = ctypes.c_int
+        lib.wf_paged_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, f32,
+                                                       wf_pool_desc, vp, vp]
+        lib.wf_paged_decode_static_scratch.restype = ctypes.c_int
         lib.wf_device_status_fetch.argtypes = [vp, vp, ctypes.c_int, vp]
         lib.wf_device_status_fetch.restype = ctypes.c_int
         lib.wf_status_string.argtypes = [ctypes.c_int]
@@ -167,6 +171,24 @@ def wf_paged_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens, 
                               int(max_q_len), int(max_seq_len), int(H_q), float(scale),
                               pool_desc(k_pool), _ptr(dev_status), _stream(stream))
     _check("wf_paged_prefill", rc)
+
+
+WF_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def wf_paged_decode_static_scratch(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len: int,
+                                   scale: float, dev_status=None, stream=None):
+    """wf_paged_decode without a caller workspace, for callers that cannot allocate
+    device memory: the library's fixed device array is the scratch.  Calls on one
+    device share that array, so they must not overlap in time."""
+    _contig(out, q, k_pool, v_pool, block_tables, seq_lens)
+    lib = load()
+    B, H_q, _ = q.shape
+    rc = lib.wf_paged_decode_static_scratch(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                            int(block_tables.shape[1]), _ptr(seq_lens), int(B), int(max_seq_len),
+                                            int(H_q), float(scale), pool_desc(k_pool), _ptr(dev_status),
+                                            _stream(stream))
+    _check("wf_paged_decode_static_scratch", rc)
 
 
 def wf_device_status_fetch(dev_status, clear: bool = True, stream=None) -> int:
