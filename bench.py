@@ -101,7 +101,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
 
@@ -292,6 +292,134 @@ class E2EDecode:
         return start.elapsed_time(end)
 
 
+class MixedWorkload:
+    """L layers of a mixed continuous-batching step at Llama-3-8B shapes: one
+    scatter of every new token (prefill and decode rows), the causal prefill of the
+    prefill requests and the decode of the decode sequences, all on one pool per layer."""
+
+    def __init__(self, pf, dc, layers: int, seed: int):
+        import torch
+        from paged_kv_cache_wf_gb300 import binding as wf
+        self.torch, self.wf = torch, wf
+        self.lib = wf.load()
+        self.pf, self.dc = pf, dc
+        g = pf.geom
+        self.L = layers
+        self.pools = [W.device_pools([pf, dc], seed=seed + 17 * l) for l in range(layers)]
+        self.pvals = [W.device_step_values(pf, seed=seed + 17 * l + 5) for l in range(layers)]
+        self.dvals = [W.device_step_values(dc, seed=seed + 17 * l + 9) for l in range(layers)]
+        self.knew = [torch.cat([a[1], b[1]]) for a, b in zip(self.pvals, self.dvals)]
+        self.vnew = [torch.cat([a[2], b[2]]) for a, b in zip(self.pvals, self.dvals)]
+        self.pouts = [torch.empty_like(v[0]) for v in self.pvals]
+        self.douts = [torch.empty_like(v[0]) for v in self.dvals]
+        self.slots = torch.from_numpy(np.concatenate([pf.new_slots(), dc.new_slots()])).cuda()
+        self.pbt = torch.from_numpy(pf.block_tables).cuda()
+        self.psl = torch.from_numpy(pf.seq_lens).cuda()
+        self.pcu = torch.from_numpy(pf.cu_q_lens).cuda()
+        self.dbt = torch.from_numpy(dc.block_tables).cuda()
+        self.dsl = torch.from_numpy(dc.seq_lens).cuda()
+        self.desc = wf.pool_desc(self.pools[0][0])
+        self.ws_bytes = wf.wf_paged_decode_workspace_size(dc.B, g.H_q, dc.max_seq_len, self.desc)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.scale = 1.0 / math.sqrt(g.D)
+        self.stream = torch.cuda.current_stream()
+        self.sp = self.stream.cuda_stream
+        self.launches_per_layer = 1 + 1 + 2
+
+    def layer(self, l, ev=None):
+        kp, vp = self.pools[l]
+        g = self.pf.geom
+        rc = self.lib.wf_reshape_and_cache(self.knew[l].data_ptr(), self.vnew[l].data_ptr(), kp.data_ptr(),
+                                           vp.data_ptr(), self.slots.data_ptr(), int(self.slots.shape[0]),
+                                           self.desc, self.status.data_ptr(), self.sp)
+        assert rc == 0, rc
+        if ev is not None:
+            ev[0].record(self.stream)
+        q = self.pvals[l][0]
+        rc = self.lib.wf_paged_prefill(self.pouts[l].data_ptr(), q.data_ptr(), kp.data_ptr(), vp.data_ptr(),
+                                       self.pbt.data_ptr(), int(self.pbt.shape[1]), self.psl.data_ptr(),
+                                       self.pcu.data_ptr(), self.pf.B, int(q.shape[0]), self.pf.max_q_len,
+                                       self.pf.max_seq_len, g.H_q, self.scale, self.desc, self.status.data_ptr(),
+                                       self.sp)
+        assert rc == 0, rc
+        if ev is not None:
+            ev[1].record(self.stream)
+        q = self.dvals[l][0]
+        rc = self.lib.wf_paged_decode(self.douts[l].data_ptr(), q.data_ptr(), kp.data_ptr(), vp.data_ptr(),
+                                      self.dbt.data_ptr(), int(self.dbt.shape[1]), self.dsl.data_ptr(), self.dc.B,
+                                      self.dc.max_seq_len, g.H_q, self.scale, self.desc, self.ws.data_ptr(),
+                                      self.ws_bytes, self.status.data_ptr(), self.sp)
+        assert rc == 0, rc
+        if ev is not None:
+            ev[2].record(self.stream)
+
+    def step(self, evs=None):
+        for l in range(self.L):
+            self.layer(l, evs.pop() if evs is not None else None)
+
+    def timed(self, steps: int):
+        torch = self.torch
+        evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps * self.L)]
+        used = list(evs)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(self.stream)
+        for _ in range(steps):
+            self.step(evs)
+        end.record(self.stream)
+        end.synchronize()
+        pre = [a.elapsed_time(b) for a, b, _ in used]
+        dec = [b.elapsed_time(c) for _, b, c in used]
+        return start.elapsed_time(end), pre, dec
+
+
+def run_mixed(args, rank, world):
+    """Secondary line: the mixed prefill + decode step (all three calls)."""
+    import torch
+    pf, dc = W.mixed_step(0)
+    g = pf.geom
+    L = args.layers if args.layers > 0 else g.L
+    wl = MixedWorkload(pf, dc, L, seed=3000 + 7919 * rank)
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    if wl.wf.wf_device_status_fetch(wl.status) != 0:
+        raise SystemExit("device status flagged an error during warm-up")
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    total_ms, pre_ms, dec_ms = wl.timed(args.steps)
+    clk = clocks.stop()
+    peaks, src = load_peaks()
+    ms_step = total_ms / args.steps
+    flops = prefill_flops(pf)
+    pre_s = statistics.mean(pre_ms) / 1e3
+    dec_s = statistics.mean(dec_ms) / 1e3
+    dbytes = decode_bytes(dc)
+    tok = int(pf.q_lens.sum()) + dc.B
+    tflops = flops / pre_s / 1e12
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    line = {
+        "metric": "mixed prefill+decode step: new tokens·layers/s", "value": world * tok * L / (ms_step / 1e3),
+        "unit": "tokens·layers/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "mixed_llama8b", "prefill_requests": pf.B, "prefill_tokens": int(pf.q_lens.sum()),
+                   "decode_sequences": dc.B, "layers": L, "model_layers": g.L, "H_q": g.H_q, "H_kv": g.H_kv,
+                   "D": g.D, "P": g.P},
+        "roofline": {"kernel": "wf_paged_prefill", "bound": "tensor", "achieved": tflops, "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": tflops / peak_t, "peak_source": src,
+                     "algorithmic_flops_per_launch": flops, "avg_launch_us": pre_s * 1e6, "traffic": None},
+        "decode_roofline": {"kernel": "wf_paged_decode", "bound": "hbm", "achieved": dbytes / dec_s / 1e9,
+                            "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                            "frac": dbytes / dec_s / 1e9 / float(peaks["hbm_gbs"]),
+                            "algorithmic_bytes_per_launch": dbytes, "avg_launch_us": dec_s * 1e6},
+        "gpu_launches": args.steps * L * wl.launches_per_layer,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # the oracle (reference arm and CPU baseline)
 # ---------------------------------------------------------------------------
@@ -389,10 +517,10 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--batch", type=int, default=231, choices=[118, 231])
-    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "gpt2", "llama1b"])
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "gpt2", "llama1b", "mixed"])
     ap.add_argument("--impl", default="wf", choices=["wf", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -422,6 +550,11 @@ def main():
     if pg is not None:
         pg.barrier()
 
+    if args.workload == "mixed":
+        run_mixed(args, rank, world)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
     lay, wname = make_layout(args)
     g = lay.geom
     L = args.layers if args.layers > 0 else g.L

@@ -7,21 +7,28 @@
 // pool and G = H_q / H_kv (weft, "Shapes and symbols").
 //
 // GB300 design:
-//   * The work unit is (sequence b, split j, group of HC KV heads).  A split is a
+//   * Work item = (sequence b, split j, group of HC <= 8 KV heads).  A split is a
 //     fixed span of positions that depends only on the pool geometry, so a
 //     sequence's result is the same whatever else is in the batch.
-//   * One producer warp streams K and V rows of the split, tile by tile
-//     (kTile positions), from HBM into a ring of shared-memory stages with the
-//     bulk-copy (TMA) engine; completion is tracked by mbarrier transaction
-//     counts, release by a second mbarrier per stage.  Rows of one block that are
-//     contiguous in the pool go in one copy.  L2 policy evict-first: KV is read once.
-//   * One consumer warp per KV head holds the head's whole GQA group (up to 8
-//     query heads): each K/V byte is read from HBM once and used G times.
-//   * q.K: a lane owns 16 (or 8) head dims of a few tile positions; partial dot
-//     products are finished with a transposing butterfly over the lanes that share
-//     the positions.  Online softmax keeps the running max and sum in fp32
-//     registers (exp2 domain, q prescaled by scale*log2 e).  P.V: a lane owns D/32
-//     output dims of every query head of the group, with packed fp32x2 FMAs.
+//   * Persistent CTAs, one per SM.  CTA c takes items c, c + grid, ... and its
+//     producer warp streams their K and V rows, tile by tile (T positions), from
+//     HBM into a ring of shared-memory stages with the bulk-copy (TMA) engine,
+//     without a pipeline restart between items.  Completion is an mbarrier
+//     transaction count; each stage also carries the tile's item description.
+//     Rows of one block that are contiguous in the pool go in one copy.  L2
+//     policy evict-first: KV is read once.
+//   * Two consumer warps per KV head, each owning half of the head dimension and
+//     the head's whole GQA group (up to 8 query heads): each K/V byte is read
+//     from HBM once and used G times.
+//       q.K: a lane owns 8 dims of a few tile positions; fp32x2 FMAs; partial dot
+//            products are finished by a transposing butterfly over the lanes that
+//            share the positions, then the two halves are added through shared
+//            memory (one named barrier per tile).
+//       softmax: running max and sum per query head in fp32 registers (exp2
+//            domain, q prescaled by scale*log2 e); both warps of a pair compute
+//            the same weights.
+//       P.V: a lane owns D/64 output dims of every query head of the group;
+//            positions are paired so one fp32x2 FMA adds two positions.
 //   * A sequence that fits in one split writes its output directly; otherwise each
 //     split leaves (m, l, o) in the workspace and the combine kernel merges them
 //     with a warp-shuffle log-sum-exp reduction.
@@ -31,7 +38,9 @@ namespace wf {
 
 namespace {
 
-constexpr int kTile = 16;  // positions per pipeline stage (one producer lane each)
+constexpr int kMaxHC = 8;     // KV heads per CTA
+constexpr int kEnd = -1;      // tile meta sentinel: no more work
+constexpr int kSpan = 128;    // positions per split
 
 struct DecodeParams {
     void* out;
@@ -44,38 +53,52 @@ struct DecodeParams {
     float2* ws_ml;   // [B, max_splits, H_q]  (running max in log2 units, sum)
     uint32_t* dev_status;
     int32_t M, B, max_seq_len, H_q, H_kv, G, N, P;
-    int32_t HC;          // KV heads per CTA (= consumer warps)
+    int32_t HC;          // KV heads per CTA
+    int32_t HG;          // head groups: H_kv / HC
     int32_t split_span;  // positions per split
     int32_t max_splits;
     int32_t stages;
     float scale_log2;    // scale * log2(e)
 };
 
+// What the producer tells the consumers about the tile in a stage.
+struct TileMeta {
+    int32_t b, split, hg, p0;
+    int32_t nvalid;   // positions in the tile; kEnd = stop
+    int32_t nsplit;   // splits of sequence b
+    int32_t first, last;
+};
+
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// Sequence-length check shared by the split and combine kernels.
 __device__ __forceinline__ bool len_ok(int len, const DecodeParams& p) {
     return len >= 1 && len <= p.max_seq_len && (int64_t)len <= (int64_t)p.M * p.P;
 }
 
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
 template <typename E, int D, int GMAX>
 struct Shape {
-    static constexpr int EPC = E::kPerChunk;                   // elements per 16-byte chunk
-    static constexpr int DPL = GMAX >= 8 ? 8 : 16;             // head dims per lane in q.K
-    static constexpr int DG = D / DPL;                         // lanes sharing one position
-    static constexpr int PS = 32 / DG;                         // positions in flight per warp
-    static constexpr int NPL = kTile / PS;                     // positions per lane per tile
-    static constexpr int CPL = DPL / EPC;                      // chunks per lane per position
-    static constexpr int NV = NPL * GMAX;                      // partial dot products per lane
-    static constexpr int VPL = D / 32;                         // output dims per lane in P.V
-    static constexpr int NSE = (kTile * GMAX + 31) / 32;       // softmax entries per lane
-    static_assert(D % DPL == 0 && 32 % DG == 0 && kTile % PS == 0, "bad decode shape");
-    static_assert(DPL % EPC == 0 && VPL % 2 == 0, "bad decode shape");
+    static constexpr int EB = E::kBytes;
+    static constexpr int T = GMAX >= 8 ? 8 : 16;                  // positions per tile
+    static constexpr int DH = D / 2;                              // dims per warp of a pair
+    static constexpr int DPL = (GMAX >= 8 && D == 64) ? 4 : 8;    // dims per lane in q.K
+    static constexpr int LB = DPL * EB < 16 ? DPL * EB : 16;      // bytes per shared load
+    static constexpr int NCH = DPL * EB / LB;                     // loads per lane per position
+    static constexpr int EPL = LB / EB;                           // elements per load
+    static constexpr int DG = DH / DPL;                           // lanes sharing a position
+    static constexpr int PS = 32 / DG;                            // positions per pass
+    static constexpr int NPL = T / PS;                            // positions per lane per tile
+    static constexpr int NV = NPL * GMAX;                         // partial dots per lane
+    static constexpr int NF = NV / DG > 0 ? NV / DG : 1;          // finished dots per lane
+    static constexpr int VPL = DH / 32;                           // P.V output dims per lane
+    static_assert(DG >= GMAX, "a lane's finished dots must belong to one query head");
+    static_assert(NPL >= 1 && T % 4 == 0 && EPL % 2 == 0 && DH % 32 == 0, "bad decode shape");
 };
 
 // Butterfly that finishes NV partial sums held by each of DG lanes (lane bits
-// [0, log2 DG)), halving the set each round while it can.  Lane ends with
-// NF = max(1, NV/DG) totals; total j of a lane has original index
+// [0, log2 DG)), halving the set each round while it can.  A lane ends with
+// NF = max(1, NV/DG) totals; total j has original index
 // j + sum_r bit_r(lane) * (NV >> (r+1)) over the halving rounds r (mask DG/2 first).
 template <int NV, int DG>
 __device__ __forceinline__ void transpose_reduce(float (&v)[NV], int lane) {
@@ -101,166 +124,263 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[NV], int lane) {
 }
 
 template <int NV, int DG>
-__device__ __forceinline__ int reduced_index(int j, int lane) {
-    int idx = j, n = NV;
+__device__ __forceinline__ int reduced_offset(int lane) {
+    int off = 0, n = NV;
 #pragma unroll
     for (int mask = DG / 2; mask >= 1; mask >>= 1) {
         if (n >= 2) {
-            if (lane & mask) idx += n / 2;
+            if (lane & mask) off += n / 2;
             n /= 2;
         }
     }
-    return idx;
+    return off;
+}
+
+// Does lane bit `mask` select the query head of a lane's finished dots?
+template <int NV, int NPL, int DG>
+__host__ __device__ constexpr bool head_bit(int mask) {
+    return mask < DG && (ilog2(DG / mask) - 1) < ilog2(NV) &&
+           (ilog2(NV) - 1 - (ilog2(DG / mask) - 1)) >= ilog2(NPL);
+}
+// Does lane bit `mask` only duplicate values (a plain butterfly round)?
+template <int NV, int DG>
+__host__ __device__ constexpr bool dup_bit(int mask) {
+    return mask < DG && (ilog2(DG / mask) - 1) >= ilog2(NV);
+}
+// A lane whose finished dots belong to query head g.
+template <int NV, int NPL, int DG>
+__device__ __forceinline__ int head_lane(int g) {
+    int lane = 0;
+#pragma unroll
+    for (int mask = DG / 2; mask >= 1; mask >>= 1) {
+        if (head_bit<NV, NPL, DG>(mask)) {
+            const int k = ilog2(NV) - 1 - (ilog2(DG / mask) - 1);  // index bit of this round
+            if ((g >> (k - ilog2(NPL))) & 1) lane |= mask;
+        }
+    }
+    return lane;
+}
+
+template <typename E, int LB>
+__device__ __forceinline__ void load_widen(const unsigned char* src, float* f) {
+    if constexpr (LB == 16) {
+        widen_chunk<E>(ld_shared_v4(src), f);
+    } else {  // 8 bytes of bf16
+        const uint2 u = ld_shared_v2(src);
+        const float2 a = bf16x2_to_float2(u.x), b = bf16x2_to_float2(u.y);
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    }
+}
+
+// One lane's VPL dims of V at one position, as fp32 (0 when `live` is false).
+template <typename E, int VPL>
+__device__ __forceinline__ void load_v(const unsigned char* src, bool live, float* f) {
+    if constexpr (E::kBytes == 2) {
+        if constexpr (VPL == 2) {
+            const uint32_t u = live ? *reinterpret_cast<const uint32_t*>(src) : 0u;
+            f[0] = __uint_as_float(u << 16);
+            f[1] = __uint_as_float(u & 0xffff0000u);
+        } else {
+            const uint32_t u = live ? (uint32_t)(*reinterpret_cast<const uint16_t*>(src)) : 0u;
+            f[0] = __uint_as_float(u << 16);
+        }
+    } else {
+        if constexpr (VPL == 2) {
+            const float2 x = live ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
+            f[0] = x.x;
+            f[1] = x.y;
+        } else {
+            f[0] = live ? *reinterpret_cast<const float*>(src) : 0.f;
+        }
+    }
 }
 
 template <typename E, int D, int GMAX>
-__global__ void __launch_bounds__(9 * 32) paged_decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, 1) paged_decode_kernel(const DecodeParams p) {
     using S = Shape<E, D, GMAX>;
-    constexpr int EB = E::kBytes;
-    const int split = blockIdx.x;
-    const int b = blockIdx.y;
-    const int hg = blockIdx.z;
+    constexpr int T = S::T;
+    constexpr int EB = S::EB;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int NW = p.HC;
+    const int NCW = 2 * p.HC;  // consumer warps
+    const int row_bytes = p.HC * D * EB;
+    const int tile_bytes = T * row_bytes;
 
-    const int len = __ldg(p.seq_lens + b);
-    if (!len_ok(len, p)) {
-        if (split == 0 && hg == 0 && threadIdx.x == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
-        return;
-    }
-    const int nsplit = (len + p.split_span - 1) / p.split_span;
-    if (split >= nsplit) return;
-    const int s0 = split * p.split_span;
-    const int s1 = min(len, s0 + p.split_span);
-    const int ntiles = (s1 - s0 + kTile - 1) / kTile;
-    const int blk0 = s0 / p.P;
-    const int nblk = (s1 - 1) / p.P - blk0 + 1;
-
-    // ---- shared memory carve-up -------------------------------------------
     extern __shared__ __align__(128) unsigned char smem[];
-    const int row_bytes = p.HC * D * EB;             // one position, this CTA's heads
-    const int tile_bytes = kTile * row_bytes;
     unsigned char* sK = smem;
-    unsigned char* sV = smem + (size_t)p.stages * tile_bytes;
+    unsigned char* sV = sK + (size_t)p.stages * tile_bytes;
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(sV + (size_t)p.stages * tile_bytes);
     uint64_t* empty_bar = full_bar + p.stages;
-    float* sS = reinterpret_cast<float*>(empty_bar + p.stages);       // [NW][kTile*GMAX]
-    int32_t* sTable = reinterpret_cast<int32_t*>(sS + NW * kTile * GMAX);
+    TileMeta* sMeta = reinterpret_cast<TileMeta*>(empty_bar + p.stages);
+    float* sX = reinterpret_cast<float*>(sMeta + p.stages);   // [HC][parity][half][32][NF]
+    float* sP = sX + p.HC * 2 * 2 * 32 * S::NF;                // [NCW][GMAX][T]
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], NW);
+            mbar_init(&empty_bar[s], NCW);
         }
         fence_mbar_init();
     }
-    const int32_t* table = p.block_tables + (int64_t)b * p.M + blk0;
-    for (int i = threadIdx.x; i < nblk; i += blockDim.x) sTable[i] = __ldg(table + i);
     __syncthreads();
 
-    if (warp == NW) {
-        // ===================== producer warp ================================
+    if (warp == NCW) {
+        // ======================= producer warp ==============================
         const uint64_t pol = l2_policy_evict_first();
-        const int64_t pool_row = (int64_t)p.H_kv * D * EB;     // bytes of one pool slot
-        const int64_t head_off = (int64_t)hg * p.HC * D * EB;  // this CTA's heads in a slot
-        const bool whole_rows = (p.HC == p.H_kv);              // slots contiguous across positions
-        int issued = 0;
-        for (int t = 0; t < ntiles; ++t) {
-            const int st = t % p.stages;
-            if (t >= p.stages) {
-                if (!mbar_wait(&empty_bar[st], ((t / p.stages) - 1) & 1)) {
+        const int64_t pool_row = (int64_t)p.H_kv * D * EB;  // bytes of one pool slot
+        const bool whole_rows = (p.HC == p.H_kv);           // slots contiguous across positions
+        int t = 0;
+        int b = 0, len_b = 0, nsp_b = -1;
+        int64_t cum = 0;  // splits of sequences before b
+        bool ok = true;
+        for (int64_t item = blockIdx.x; ok; item += gridDim.x) {
+            const int64_t u = item / p.HG;
+            const int hg = (int)(item % p.HG);
+            while (b < p.B) {
+                if (nsp_b < 0) {
+                    len_b = __ldg(p.seq_lens + b);
+                    if (len_ok(len_b, p)) {
+                        nsp_b = (len_b + p.split_span - 1) / p.split_span;
+                    } else {
+                        nsp_b = 0;
+                        if (lane == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
+                    }
+                }
+                if (u < cum + nsp_b) break;
+                cum += nsp_b;
+                ++b;
+                nsp_b = -1;
+            }
+            if (b >= p.B) break;
+            const int split = (int)(u - cum);
+            const int s0 = split * p.split_span;
+            const int s1 = min(len_b, s0 + p.split_span);
+            const int ntiles = (s1 - s0 + T - 1) / T;
+            const int32_t* table = p.block_tables + (int64_t)b * p.M;
+            const int64_t head_off = (int64_t)hg * p.HC * D * EB;
+            for (int j = 0; j < ntiles; ++j, ++t) {
+                const int st = t % p.stages;
+                if (t >= p.stages && !mbar_wait(&empty_bar[st], ((t / p.stages) - 1) & 1)) {
                     if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+                    ok = false;
                     break;
                 }
+                const int p0 = s0 + j * T;
+                const int nvalid = min(T, s1 - p0);
+                const int pos = p0 + lane;
+                const bool valid = lane < nvalid;
+                int blk = 0, off = 0;
+                if (valid) {
+                    blk = __ldg(table + pos / p.P);
+                    off = pos % p.P;
+                }
+                const bool okb = valid && (unsigned)blk < (unsigned)p.N;
+                if (valid && !okb && (lane == 0 || off == 0)) report(p.dev_status, WF_DEV_BAD_BLOCK);
+                const unsigned okmask = __ballot_sync(0xffffffffu, okb);
+                const uint32_t bytes = (uint32_t)__popc(okmask) * (uint32_t)row_bytes * 2u;
+                if (lane == 0) {
+                    TileMeta m;
+                    m.b = b; m.split = split; m.hg = hg; m.p0 = p0; m.nvalid = nvalid; m.nsplit = nsp_b;
+                    m.first = (j == 0); m.last = (j == ntiles - 1);
+                    sMeta[st] = m;
+                    mbar_arrive_expect_tx(&full_bar[st], bytes);
+                }
+                __syncwarp();
+                const bool start = okb && (!whole_rows || lane == 0 || off == 0);
+                if (start) {
+                    const int run = whole_rows ? min(p.P - off, nvalid - lane) : 1;
+                    const int64_t src = ((int64_t)blk * p.P + off) * pool_row + head_off;
+                    bulk_g2s(sK + (size_t)st * tile_bytes + lane * row_bytes, p.k_pool + src,
+                             (uint32_t)(run * row_bytes), &full_bar[st], pol);
+                    bulk_g2s(sV + (size_t)st * tile_bytes + lane * row_bytes, p.v_pool + src,
+                             (uint32_t)(run * row_bytes), &full_bar[st], pol);
+                }
             }
-            const int p0 = s0 + t * kTile;
-            const int nvalid = min(kTile, s1 - p0);
-            const int pos = p0 + lane;
-            const bool valid = lane < nvalid;
-            int blk = 0, off = 0;
-            if (valid) {
-                blk = sTable[pos / p.P - blk0];
-                off = pos % p.P;
+        }
+        if (ok) {  // tell the consumers to stop
+            const int st = t % p.stages;
+            if (t < p.stages || mbar_wait(&empty_bar[st], ((t / p.stages) - 1) & 1)) {
+                if (lane == 0) {
+                    sMeta[st].nvalid = kEnd;
+                    mbar_arrive_expect_tx(&full_bar[st], 0);
+                }
+                ++t;
+            } else if (lane == 0) {
+                report(p.dev_status, WF_DEV_TIMEOUT);
             }
-            const bool ok = valid && (unsigned)blk < (unsigned)p.N;
-            if (valid && !ok && (lane == 0 || off == 0)) report(p.dev_status, WF_DEV_BAD_BLOCK);
-            const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-            const uint32_t bytes = (uint32_t)__popc(okmask) * (uint32_t)row_bytes * 2u;
-            if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], bytes);
-            __syncwarp();
-            const bool start = ok && (!whole_rows || lane == 0 || off == 0);
-            if (start) {
-                const int run = whole_rows ? min(p.P - off, nvalid - lane) : 1;
-                const int64_t src = ((int64_t)blk * p.P + off) * pool_row + head_off;
-                bulk_g2s(sK + (size_t)st * tile_bytes + lane * row_bytes, p.k_pool + src,
-                         (uint32_t)(run * row_bytes), &full_bar[st], pol);
-                bulk_g2s(sV + (size_t)st * tile_bytes + lane * row_bytes, p.v_pool + src,
-                         (uint32_t)(run * row_bytes), &full_bar[st], pol);
-            }
-            ++issued;
         }
         // Never leave with copies in flight: the last stages' fills must have landed.
         if (lane == 0) {
-            const int first = issued > p.stages ? issued - p.stages : 0;
-            for (int t = first; t < issued; ++t)
-                mbar_wait(&full_bar[t % p.stages], (t / p.stages) & 1, 1u << 20);
+            const int first = t > p.stages ? t - p.stages : 0;
+            for (int tt = first; tt < t; ++tt) mbar_wait(&full_bar[tt % p.stages], (tt / p.stages) & 1, 1u << 20);
         }
         return;
     }
 
-    // ======================= consumer warps =================================
+    // ========================= consumer warps ===============================
+    const int pair = warp >> 1;   // KV head within the CTA
+    const int half = warp & 1;    // which half of the head dimension
     const int dg = lane % S::DG;
     const int ps = lane / S::DG;
-    const int h_local = warp;                      // KV head within the CTA
-    const int hq0 = (hg * p.HC + h_local) * p.G;   // first query head of the group
     const int G = p.G;
+    float* sPw = sP + warp * GMAX * T;
+    float* sXp = sX + pair * (2 * 2 * 32 * S::NF);
+    const int off_r = reduced_offset<S::NV, S::DG>(lane);
+    const int g_lane = off_r / S::NPL;  // query head of this lane's finished dots
 
-    // q of the group, the lane's chunks, prescaled into the exp2 domain
-    float2 q2[GMAX][S::CPL][S::EPC / 2];
-#pragma unroll
-    for (int g = 0; g < GMAX; ++g) {
-#pragma unroll
-        for (int k = 0; k < S::CPL; ++k) {
-            const int c = dg + S::DG * ((k + ps) % S::CPL);
-            float f[S::EPC];
-            if (g < G) {
-                const char* src = static_cast<const char*>(p.q) +
-                                  (((int64_t)b * p.H_q + hq0 + g) * D + c * S::EPC) * EB;
-                widen_chunk<E>(*reinterpret_cast<const uint4*>(src), f);
-            } else {
-#pragma unroll
-                for (int e = 0; e < S::EPC; ++e) f[e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < S::EPC / 2; ++e)
-                q2[g][k][e] = make_float2(f[2 * e] * p.scale_log2, f[2 * e + 1] * p.scale_log2);
-        }
-    }
+    float2 q2[GMAX][S::DPL / 2];
+    float2 acc[GMAX][S::VPL];
+    float m_run = -INFINITY, l_run = 0.f;
+    int hq0 = 0;
 
-    float2 acc[GMAX][S::VPL / 2];
-#pragma unroll
-    for (int g = 0; g < GMAX; ++g)
-#pragma unroll
-        for (int v = 0; v < S::VPL / 2; ++v) acc[g][v] = make_float2(0.f, 0.f);
-    float m_run = -INFINITY;  // running max of head (lane % GMAX), log2 units
-    float l_run = 0.f;        // this lane's share of that head's running sum
-    float* sSw = sS + warp * kTile * GMAX;
-    bool timed_out = false;
-
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = 0;; ++t) {
         const int st = t % p.stages;
         if (!mbar_wait(&full_bar[st], (t / p.stages) & 1)) {
             if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
-            timed_out = true;
-            break;
+            return;
         }
-        const int p0 = s0 + t * kTile;
-        const int nvalid = min(kTile, s1 - p0);
-        const unsigned char* tK = sK + (size_t)st * tile_bytes + h_local * D * EB;
-        const unsigned char* tV = sV + (size_t)st * tile_bytes + h_local * D * EB;
+        const TileMeta mt = sMeta[st];
+        if (mt.nvalid == kEnd) break;
+        const int nvalid = mt.nvalid;
+        if (mt.first) {
+            hq0 = (mt.hg * p.HC + pair) * G;
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+#pragma unroll
+                for (int k = 0; k < S::NCH; ++k) {
+                    const int c = dg + S::DG * ((k + ps) % S::NCH);
+                    float f[S::EPL];
+                    if (g < G) {
+                        const char* src = static_cast<const char*>(p.q) +
+                                          (((int64_t)mt.b * p.H_q + hq0 + g) * D + half * S::DH) * EB + c * S::LB;
+                        if constexpr (S::LB == 16) {
+                            widen_chunk<E>(*reinterpret_cast<const uint4*>(src), f);
+                        } else {
+                            const uint2 u = *reinterpret_cast<const uint2*>(src);
+                            const float2 a = bf16x2_to_float2(u.x), bb = bf16x2_to_float2(u.y);
+                            f[0] = a.x; f[1] = a.y; f[2] = bb.x; f[3] = bb.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < S::EPL; ++e) f[e] = 0.f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < S::EPL / 2; ++e)
+                        q2[g][k * S::EPL / 2 + e] =
+                            make_float2(f[2 * e] * p.scale_log2, f[2 * e + 1] * p.scale_log2);
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g)
+#pragma unroll
+                for (int v = 0; v < S::VPL; ++v) acc[g][v] = make_float2(0.f, 0.f);
+            m_run = -INFINITY;
+            l_run = 0.f;
+        }
+        const unsigned char* tK = sK + (size_t)st * tile_bytes + pair * D * EB + half * S::DH * EB;
+        const unsigned char* tV = sV + (size_t)st * tile_bytes + pair * D * EB + half * S::DH * EB;
 
-        // ---- scores: q . K for the lane's positions, all heads of the group --
+        // ---- q . K over this warp's half of D --------------------------------
         float2 part[GMAX][S::NPL];
 #pragma unroll
         for (int g = 0; g < GMAX; ++g)
@@ -269,18 +389,17 @@ __global__ void __launch_bounds__(9 * 32) paged_decode_split_kernel(const Decode
 #pragma unroll
         for (int i = 0; i < S::NPL; ++i) {
             const int pl = ps + S::PS * i;
-            if (pl < nvalid) {
 #pragma unroll
-                for (int k = 0; k < S::CPL; ++k) {
-                    const int c = dg + S::DG * ((k + ps) % S::CPL);
-                    float f[S::EPC];
-                    widen_chunk<E>(ld_shared_v4(tK + pl * row_bytes + c * 16), f);
+            for (int k = 0; k < S::NCH; ++k) {
+                const int c = dg + S::DG * ((k + ps) % S::NCH);
+                float f[S::EPL];
+                load_widen<E, S::LB>(tK + pl * row_bytes + c * S::LB, f);
 #pragma unroll
-                    for (int e = 0; e < S::EPC / 2; ++e) {
-                        const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
+                for (int e = 0; e < S::EPL / 2; ++e) {
+                    const float2 kk = make_float2(f[2 * e], f[2 * e + 1]);
 #pragma unroll
-                        for (int g = 0; g < GMAX; ++g) part[g][i] = ffma2(q2[g][k][e], kk, part[g][i]);
-                    }
+                    for (int g = 0; g < GMAX; ++g)
+                        part[g][i] = ffma2(q2[g][k * S::EPL / 2 + e], kk, part[g][i]);
                 }
             }
         }
@@ -290,132 +409,110 @@ __global__ void __launch_bounds__(9 * 32) paged_decode_split_kernel(const Decode
 #pragma unroll
             for (int i = 0; i < S::NPL; ++i) v[g * S::NPL + i] = part[g][i].x + part[g][i].y;
         transpose_reduce<S::NV, S::DG>(v, lane);
-        constexpr int NF = S::NV / S::DG > 0 ? S::NV / S::DG : 1;
-#pragma unroll
-        for (int j = 0; j < NF; ++j) {
-            const int idx = reduced_index<S::NV, S::DG>(j, lane);
-            const int g = idx / S::NPL;
-            const int pl = ps + S::PS * (idx % S::NPL);
-            sSw[pl * GMAX + g] = v[j];
-        }
-        __syncwarp();
 
-        // ---- online softmax (per query head, exp2 domain) --------------------
-        float sv[S::NSE];
-        float mt = -INFINITY;
+        // ---- add the other half of D (the partner warp) ------------------------
+        {
+            const int par = t & 1;
+            float* mine = sXp + ((par * 2 + half) * 32 + lane) * S::NF;
+            const float* theirs = sXp + ((par * 2 + (1 - half)) * 32 + lane) * S::NF;
 #pragma unroll
-        for (int k = 0; k < S::NSE; ++k) {
-            const int e = lane + 32 * k;
-            const bool live = e < kTile * GMAX && (e / GMAX) < nvalid;
-            sv[k] = live ? sSw[e] : -INFINITY;
-            mt = fmaxf(mt, sv[k]);
+            for (int j = 0; j < S::NF; ++j) mine[j] = v[j];
+            named_bar_sync(1 + pair, 64);
+#pragma unroll
+            for (int j = 0; j < S::NF; ++j) v[j] += theirs[j];
+        }
+
+        // ---- online softmax for query head g_lane -------------------------------
+        float s[S::NF];
+        int plj[S::NF];
+        float mtile = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < S::NF; ++j) {
+            plj[j] = ps + S::PS * ((off_r + j) % S::NPL);
+            s[j] = plj[j] < nvalid ? v[j] : -INFINITY;
+            mtile = fmaxf(mtile, s[j]);
         }
 #pragma unroll
-        for (int mask = GMAX; mask < 32; mask <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, mask));
-        const float m_new = fmaxf(m_run, mt);
-        const float alpha = exp2f(m_run - m_new);   // 0 on the first tile
+        for (int mask = 1; mask < 32; mask <<= 1)
+            if (!head_bit<S::NV, S::NPL, S::DG>(mask)) mtile = fmaxf(mtile, __shfl_xor_sync(0xffffffffu, mtile, mask));
+        const float m_new = fmaxf(m_run, mtile);
+        const float alpha = exp2f(m_run - m_new);  // 0 on an item's first tile
         float psum = 0.f;
 #pragma unroll
-        for (int k = 0; k < S::NSE; ++k) {
-            const int e = lane + 32 * k;
-            const float pe = exp2f(sv[k] - m_new);  // exp2(-inf) = 0 for dead entries
-            psum += pe;
-            if (e < kTile * GMAX) sSw[e] = pe;
+        for (int j = 0; j < S::NF; ++j) {
+            const float pj = exp2f(s[j] - m_new);   // 0 for positions past the tile end
+            psum += pj;
+            sPw[g_lane * T + plj[j]] = pj;
         }
         l_run = l_run * alpha + psum;
         m_run = m_new;
         float a[GMAX];
 #pragma unroll
-        for (int g = 0; g < GMAX; ++g) a[g] = __shfl_sync(0xffffffffu, alpha, g);
+        for (int g = 0; g < GMAX; ++g) a[g] = __shfl_sync(0xffffffffu, alpha, head_lane<S::NV, S::NPL, S::DG>(g));
         __syncwarp();
 #pragma unroll
         for (int g = 0; g < GMAX; ++g)
 #pragma unroll
-            for (int vv = 0; vv < S::VPL / 2; ++vv) {
-                acc[g][vv].x *= a[g];
-                acc[g][vv].y *= a[g];
-            }
+            for (int vv = 0; vv < S::VPL; ++vv) acc[g][vv] = make_float2(acc[g][vv].x * a[g], acc[g][vv].y * a[g]);
 
-        // ---- P . V ----------------------------------------------------------
-        for (int pl = 0; pl < nvalid; ++pl) {
-            float pw[GMAX];
-            if constexpr (GMAX >= 4) {
+        // ---- P . V, two positions per fp32x2 FMA ------------------------------
+        const unsigned char* vcol = tV + lane * S::VPL * EB;
 #pragma unroll
-                for (int g4 = 0; g4 < GMAX; g4 += 4) {
-                    const float4 w4 = ld_shared_f4(sSw + pl * GMAX + g4);
-                    pw[g4] = w4.x; pw[g4 + 1] = w4.y; pw[g4 + 2] = w4.z; pw[g4 + 3] = w4.w;
-                }
-            } else {
+        for (int pl = 0; pl < T; pl += 4) {
+            float vf[4][S::VPL];
 #pragma unroll
-                for (int g = 0; g < GMAX; ++g) pw[g] = sSw[pl * GMAX + g];
-            }
-            float vf[S::VPL];
-            const unsigned char* src = tV + pl * row_bytes + lane * S::VPL * EB;
-            if constexpr (EB == 2) {
-                if constexpr (S::VPL == 4) {
-                    const uint2 u = *reinterpret_cast<const uint2*>(src);
-                    const float2 x = bf16x2_to_float2(u.x), y = bf16x2_to_float2(u.y);
-                    vf[0] = x.x; vf[1] = x.y; vf[2] = y.x; vf[3] = y.y;
-                } else {
-                    const float2 x = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(src));
-                    vf[0] = x.x; vf[1] = x.y;
-                }
-            } else {
-                if constexpr (S::VPL == 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(src);
-                    vf[0] = x.x; vf[1] = x.y; vf[2] = x.z; vf[3] = x.w;
-                } else {
-                    const float2 x = *reinterpret_cast<const float2*>(src);
-                    vf[0] = x.x; vf[1] = x.y;
+            for (int k = 0; k < 4; ++k) load_v<E, S::VPL>(vcol + (pl + k) * row_bytes, pl + k < nvalid, vf[k]);
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+                const float4 w = ld_shared_f4(sPw + g * T + pl);
+#pragma unroll
+                for (int vv = 0; vv < S::VPL; ++vv) {
+                    acc[g][vv] = ffma2(make_float2(w.x, w.y), make_float2(vf[0][vv], vf[1][vv]), acc[g][vv]);
+                    acc[g][vv] = ffma2(make_float2(w.z, w.w), make_float2(vf[2][vv], vf[3][vv]), acc[g][vv]);
                 }
             }
-#pragma unroll
-            for (int g = 0; g < GMAX; ++g)
-#pragma unroll
-                for (int vv = 0; vv < S::VPL / 2; ++vv)
-                    acc[g][vv] = ffma2(make_float2(pw[g], pw[g]),
-                                       make_float2(vf[2 * vv], vf[2 * vv + 1]), acc[g][vv]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);
-    }
-    if (timed_out) return;
 
-    // ---- finish: per-head sums, then output or partial ------------------------
+        if (mt.last) {
+            // ---- finish the item: per-head sums, then output or partial ----------
+            float lt = l_run;
 #pragma unroll
-    for (int mask = GMAX; mask < 32; mask <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, mask);
-    float l_h[GMAX], m_h[GMAX];
+            for (int mask = 1; mask < 32; mask <<= 1)
+                if (!head_bit<S::NV, S::NPL, S::DG>(mask) && !dup_bit<S::NV, S::DG>(mask))
+                    lt += __shfl_xor_sync(0xffffffffu, lt, mask);
+            float Lh[GMAX], Mh[GMAX];
 #pragma unroll
-    for (int g = 0; g < GMAX; ++g) {
-        l_h[g] = __shfl_sync(0xffffffffu, l_run, g);
-        m_h[g] = __shfl_sync(0xffffffffu, m_run, g);
-    }
-    if (nsplit == 1) {
-#pragma unroll
-        for (int g = 0; g < GMAX; ++g) {
-            if (g < G) {
-                const float inv = 1.f / l_h[g];
-                float o[S::VPL];
-#pragma unroll
-                for (int vv = 0; vv < S::VPL / 2; ++vv) {
-                    o[2 * vv] = acc[g][vv].x * inv;
-                    o[2 * vv + 1] = acc[g][vv].y * inv;
-                }
-                char* dst = static_cast<char*>(p.out) +
-                            (((int64_t)b * p.H_q + hq0 + g) * D + lane * S::VPL) * EB;
-                store_out<E, S::VPL>(dst, o);
+            for (int g = 0; g < GMAX; ++g) {
+                const int src = head_lane<S::NV, S::NPL, S::DG>(g);
+                Lh[g] = __shfl_sync(0xffffffffu, lt, src);
+                Mh[g] = __shfl_sync(0xffffffffu, m_run, src);
             }
-        }
-    } else {
-        const int64_t base = ((int64_t)b * p.max_splits + split) * p.H_q + hq0;
+            const int dcol = half * S::DH + lane * S::VPL;
+            if (mt.nsplit == 1) {
 #pragma unroll
-        for (int g = 0; g < GMAX; ++g) {
-            if (g < G) {
-                float* dst = p.ws_o + (base + g) * D + lane * S::VPL;
+                for (int g = 0; g < GMAX; ++g) {
+                    if (g < G) {
+                        const float inv = 1.f / Lh[g];
+                        float o[S::VPL];
 #pragma unroll
-                for (int vv = 0; vv < S::VPL / 2; ++vv)
-                    reinterpret_cast<float2*>(dst)[vv] = acc[g][vv];
-                if (lane == 0) p.ws_ml[base + g] = make_float2(m_h[g], l_h[g]);
+                        for (int vv = 0; vv < S::VPL; ++vv) o[vv] = (acc[g][vv].x + acc[g][vv].y) * inv;
+                        char* dst = static_cast<char*>(p.out) + (((int64_t)mt.b * p.H_q + hq0 + g) * D + dcol) * EB;
+                        store_out<E, S::VPL>(dst, o);
+                    }
+                }
+            } else {
+                const int64_t base = ((int64_t)mt.b * p.max_splits + mt.split) * p.H_q + hq0;
+#pragma unroll
+                for (int g = 0; g < GMAX; ++g) {
+                    if (g < G) {
+                        float* dst = p.ws_o + (base + g) * D + dcol;
+#pragma unroll
+                        for (int vv = 0; vv < S::VPL; ++vv) dst[vv] = acc[g][vv].x + acc[g][vv].y;
+                        if (half == 0 && lane == 0) p.ws_ml[base + g] = make_float2(Mh[g], Lh[g]);
+                    }
+                }
             }
         }
     }
@@ -423,7 +520,8 @@ __global__ void __launch_bounds__(9 * 32) paged_decode_split_kernel(const Decode
 
 // Merge the splits of every (sequence, query head) with more than one split:
 //   out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j.
-// One warp per (b, query head); lanes own D/32 output dims.
+// One warp per (b, query head); lanes own D/32 output dims; the split loop keeps
+// several independent loads in flight.
 template <typename E, int D>
 __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p) {
     constexpr int VPL = D / 32;
@@ -441,27 +539,32 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
 #pragma unroll
     for (int mask = 16; mask >= 1; mask >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
     float den = 0.f;
-    for (int j = lane; j < n; j += 32) {
-        const float2 ml = p.ws_ml[base + (int64_t)j * p.H_q];
-        den += exp2f(ml.x - mx) * ml.y;
-    }
-#pragma unroll
-    for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(0xffffffffu, den, mask);
     float o[VPL];
 #pragma unroll
     for (int k = 0; k < VPL; ++k) o[k] = 0.f;
-    for (int j = 0; j < n; ++j) {
-        const int64_t row = base + (int64_t)j * p.H_q;
-        const float w = exp2f(p.ws_ml[row].x - mx);
-        const float* src = p.ws_o + row * D + lane * VPL;
-        if constexpr (VPL == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src);
-            o[0] += w * x.x; o[1] += w * x.y; o[2] += w * x.z; o[3] += w * x.w;
-        } else {
-            const float2 x = *reinterpret_cast<const float2*>(src);
-            o[0] += w * x.x; o[1] += w * x.y;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        float wl = 0.f;
+        if (j0 + lane < n) {
+            const float2 ml = p.ws_ml[base + (int64_t)(j0 + lane) * p.H_q];
+            wl = exp2f(ml.x - mx);
+            den += wl * ml.y;
+        }
+        const int cnt = min(32, n - j0);
+#pragma unroll 8
+        for (int jj = 0; jj < cnt; ++jj) {
+            const float w = __shfl_sync(0xffffffffu, wl, jj);
+            const float* src = p.ws_o + (base + (int64_t)(j0 + jj) * p.H_q) * D + lane * VPL;
+            if constexpr (VPL == 4) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+                o[0] += w * x.x; o[1] += w * x.y; o[2] += w * x.z; o[3] += w * x.w;
+            } else {
+                const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+                o[0] += w * x.x; o[1] += w * x.y;
+            }
         }
     }
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(0xffffffffu, den, mask);
     const float inv = 1.f / den;
 #pragma unroll
     for (int k = 0; k < VPL; ++k) o[k] *= inv;
@@ -476,12 +579,31 @@ int pow2_at_least(int x) {
 }
 
 template <typename E, int D, int GMAX>
-cudaError_t launch_typed(const DecodeParams& p, const DecodeGeometry& g, cudaStream_t stream) {
-    auto split = paged_decode_split_kernel<E, D, GMAX>;
-    cudaError_t err = allow_dynamic_smem((const void*)split, g.smem_bytes);
+int smem_bytes_for(int hc, int stages) {
+    using S = Shape<E, D, GMAX>;
+    const int tile_bytes = S::T * hc * D * S::EB;
+    return stages * (2 * tile_bytes + 16 + (int)sizeof(TileMeta)) + hc * 2 * 2 * 32 * S::NF * 4 +
+           2 * hc * GMAX * S::T * 4;
+}
+
+template <typename E, int D, int GMAX>
+int pick_stages(int hc) {
+    constexpr int kBudget = 216 * 1024;
+    int st = 8;
+    while (st > 2 && smem_bytes_for<E, D, GMAX>(hc, st) > kBudget) --st;
+    return st;
+}
+
+template <typename E, int D, int GMAX>
+cudaError_t launch_typed(DecodeParams& p, cudaStream_t stream) {
+    auto kern = paged_decode_kernel<E, D, GMAX>;
+    p.stages = pick_stages<E, D, GMAX>(p.HC);
+    const int smem = smem_bytes_for<E, D, GMAX>(p.HC, p.stages);
+    cudaError_t err = allow_dynamic_smem((const void*)kern, smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(p.max_splits, p.B, p.H_kv / p.HC);
-    split<<<grid, (p.HC + 1) * 32, g.smem_bytes, stream>>>(p);
+    const int64_t items = (int64_t)p.B * p.max_splits * p.HG;
+    const int grid = (int)(items < num_sms() ? items : num_sms());
+    kern<<<grid, (2 * p.HC + 1) * 32, smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (p.max_splits > 1) {
@@ -493,12 +615,12 @@ cudaError_t launch_typed(const DecodeParams& p, const DecodeGeometry& g, cudaStr
 }
 
 template <typename E, int D>
-cudaError_t launch_group(const DecodeParams& p, const DecodeGeometry& g, cudaStream_t stream) {
-    switch (g.gmax) {
-        case 1: return launch_typed<E, D, 1>(p, g, stream);
-        case 2: return launch_typed<E, D, 2>(p, g, stream);
-        case 4: return launch_typed<E, D, 4>(p, g, stream);
-        default: return launch_typed<E, D, 8>(p, g, stream);
+cudaError_t launch_group(DecodeParams& p, int gmax, cudaStream_t stream) {
+    switch (gmax) {
+        case 1: return launch_typed<E, D, 1>(p, stream);
+        case 2: return launch_typed<E, D, 2>(p, stream);
+        case 4: return launch_typed<E, D, 4>(p, stream);
+        default: return launch_typed<E, D, 8>(p, stream);
     }
 }
 
@@ -510,24 +632,18 @@ bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeomet
     if (G < 1 || G > 8) return false;
     if (pool.head_dim != 64 && pool.head_dim != 128) return false;
     int hc = 1;
-    for (int c = 8; c >= 1; --c)
-        if (pool.num_kv_heads % c == 0) { hc = c; break; }
-    const int eb = dtype_bytes(pool.dtype);
-    const int row_bytes = hc * pool.head_dim * eb;
-    const int stage_bytes = 2 * kTile * row_bytes;  // K + V
-    int stages = (192 * 1024) / stage_bytes;
-    if (stages < 2) stages = 2;
-    if (stages > 6) stages = 6;
-    const int gmax = pow2_at_least(G);
-    const int span = 128;
-    const int table_ints = span / 1 + 2;  // P = 1 worst case: one entry per position
-    g->split_span = span;
-    g->tile = kTile;
-    g->stages = stages;
-    g->consumer_warps = hc;
+    for (int c = kMaxHC; c >= 1; --c)
+        if (pool.num_kv_heads % c == 0) {
+            hc = c;
+            break;
+        }
+    g->split_span = kSpan;
+    g->tile = G > 4 ? 8 : 16;
+    g->stages = 0;  // chosen per kernel instance at launch
+    g->consumer_warps = 2 * hc;
     g->heads_per_warp = 1;
-    g->gmax = gmax;
-    g->smem_bytes = stages * stage_bytes + 2 * stages * 8 + hc * kTile * gmax * 4 + table_ints * 4;
+    g->gmax = pow2_at_least(G);
+    g->smem_bytes = 0;
     return true;
 }
 
@@ -565,21 +681,35 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
     p.G = num_q_heads / pool.num_kv_heads;
     p.N = pool.num_blocks;
     p.P = pool.block_size;
-    p.HC = g.consumer_warps;
+    p.HC = g.consumer_warps / 2;
+    p.HG = pool.num_kv_heads / p.HC;
     p.split_span = g.split_span;
     p.max_splits = (max_seq_len + g.split_span - 1) / g.split_span;
-    p.stages = g.stages;
+    p.stages = 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int64_t rows = (int64_t)B * p.max_splits * num_q_heads;
     const int64_t o_bytes = ((rows * pool.head_dim * 4 + 255) / 256) * 256;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
-    if (pool.dtype == WF_DTYPE_F32) {
-        return pool.head_dim == 64 ? launch_group<F32, 64>(p, g, stream)
-                                   : launch_group<F32, 128>(p, g, stream);
+    const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
+    if (decode_tc_supported(pool, num_q_heads) && slots <= INT32_MAX) {
+        cudaError_t err = launch_paged_decode_tc(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens,
+                                                 B, max_seq_len, num_q_heads, scale, pool, p.ws_o, p.ws_ml,
+                                                 p.max_splits, dev_status, stream);
+        if (err != cudaSuccess) return err;
+        if (p.max_splits > 1) {
+            dim3 cgrid((p.H_q + 3) / 4, p.B);
+            paged_decode_combine_kernel<BF16, 128><<<cgrid, 128, 0, stream>>>(p);
+            err = cudaGetLastError();
+        }
+        return err;
     }
-    return pool.head_dim == 64 ? launch_group<BF16, 64>(p, g, stream)
-                               : launch_group<BF16, 128>(p, g, stream);
+    if (pool.dtype == WF_DTYPE_F32) {
+        return pool.head_dim == 64 ? launch_group<F32, 64>(p, g.gmax, stream)
+                                   : launch_group<F32, 128>(p, g.gmax, stream);
+    }
+    return pool.head_dim == 64 ? launch_group<BF16, 64>(p, g.gmax, stream)
+                               : launch_group<BF16, 128>(p, g.gmax, stream);
 }
 
 }  // namespace wf

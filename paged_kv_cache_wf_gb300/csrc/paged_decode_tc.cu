@@ -1,0 +1,514 @@
+// paged_decode_tc.cu -- paged decode on the 5th-generation tensor cores, for bf16
+// pools with H_kv = 8 KV heads, D = 128, a block size that is a multiple of 16
+// and GQA groups of 2 or 4 (H_q = 16 or 32).
+//
+// Same contract and split-K structure as the CUDA-core decode in
+// paged_decode.cu (ember, "The core idea"; tiny-vllm-py, "KV Cache"; weft,
+// "Shapes and symbols"): a work item is (sequence b, split of 128 positions), the
+// split boundaries depend only on the pool geometry, and the items of a
+// multi-split sequence leave (m, l, o) partials for the combine kernel.
+//
+// Why tensor cores: per KV byte the GQA group needs 2 FMAs plus a widening; on
+// CUDA cores that instruction stream, not HBM, limits decode.  Here a tile is one
+// 16-position run of a block for all 8 KV heads -- 128 rows r = (head, position)
+// -- and the group's work is two dense products issued by one thread:
+//     S^T[128 rows x H_q]  = K[128 rows x 128 d] . Q^T[128 d x H_q]
+//     O^T[128 d x H_q]     = V^T[128 d x 128 rows] . P^T[128 rows x H_q]
+// with bf16 operands and fp32 accumulators in tensor memory.  Row r only belongs
+// to the G query heads of its KV head: S entries outside that diagonal block are
+// ignored and P^T is block-diagonal (its off-diagonal entries stay zero).
+//
+// Loads: the K and V pools are described to the TMA unit as (d, slot, head) so
+// that one 16-slot box of all 8 heads lands as 8 contiguous 16-row, 128-byte-
+// swizzled head tiles, i.e. the UMMA K-major layout with rows (head, position).
+// A tile is 4 boxes of 16 KB (K and V, two 64-wide halves of D), each issued by
+// its own producer lane: the copy engine keeps one request per issuing thread in
+// flight, so spreading large copies over lanes is what reaches HBM bandwidth.
+//
+// CTA (persistent, one per SM), 6 warps:
+//   warp 0   producer (TMA): tiles into a 3-stage ring; q of an item into one of two
+//            q buffers; mbarrier transaction counts mark arrival.
+//   warp 1   MMA issuer: S(t) into one of two TMEM S buffers, then O(t-1) = V^T P^T
+//            into one of two TMEM O buffers; commits free stages and buffers.
+//   warps 2-5  (thread i):  (a) as the owner of head dim d = i, accumulates the
+//            previous tile's O^T row into fp32 registers with the per-head rescale
+//            factors, and at the end of an item stores the output or the partial;
+//            (b) as the owner of row i = (head i/16, position i%16), runs the online
+//            softmax of the current tile for the head's G query heads (reductions
+//            over the 16 positions stay inside a half-warp) and writes P^T as bf16.
+#include <cuda.h>
+
+#include "wf_internal.h"
+
+namespace wf {
+
+namespace {
+
+constexpr int kRows = 128;       // MMA M: 8 heads x 16 positions (and D = 128 for P.V)
+constexpr int kHeads = 8;        // KV heads per tile
+constexpr int kPosT = 16;        // positions per tile
+constexpr int kSpanTc = 128;     // positions per item (split)
+constexpr int kD = 128;
+constexpr int kNq = 32;          // max H_q handled (MMA N, padded to a multiple of 16)
+constexpr int kStages = 3;
+constexpr int kEndTile = -1;
+constexpr int kHalf = kRows * 128;             // one 64-wide half of a K or V tile: 16 KB
+constexpr int kStageBytes = 4 * kHalf;         // K0 K1 V0 V1
+constexpr int kQHalf = kNq * 128;              // one half of q: 32 rows x 128 B
+constexpr int kQBytes = 2 * kQHalf;
+constexpr int kPHalf = kNq * 128;              // one 64-row half of P^T (32 q rows x 128 B)
+constexpr int kPBytes = 2 * kPHalf;
+
+struct TcParams {
+    void* out;
+    float* ws_o;
+    float2* ws_ml;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    uint32_t* dev_status;
+    int32_t M, B, max_seq_len, H_q, H_kv, G, N, P, max_splits;
+    float scale_log2;
+};
+
+struct TcMeta {
+    int32_t b, split, nsplit, p0, nvalid, first, last, item;
+};
+
+struct TcSmem {  // byte offsets from the 1024-aligned base
+    static constexpr int stage = 0;
+    static constexpr int qbuf = kStages * kStageBytes;
+    static constexpr int pbuf = qbuf + 2 * kQBytes;
+    static constexpr int bars = pbuf + 2 * kPBytes;
+    // full[3] empty[3] s_full[2] s_free[2] p_full[2] o_full[2] o_free[2] q_free[2]
+    static constexpr int nbars = 2 * kStages + 12;
+    static constexpr int meta = bars + nbars * 8;
+    static constexpr int alpha = meta + kStages * (int)sizeof(TcMeta);  // [2][kNq]
+    static constexpr int lbuf = alpha + 2 * kNq * 4;                    // [2][kNq]
+    static constexpr int mbuf = lbuf + 2 * kNq * 4;                     // [2][kNq]
+    static constexpr int tmem_slot = mbuf + 2 * kNq * 4;
+    static constexpr int total = tmem_slot + 16;
+};
+static_assert(TcSmem::total + 1024 <= 232448, "tensor-core decode exceeds shared memory");
+
+__device__ __forceinline__ unsigned char* stage_k(unsigned char* base, int st, int c) {
+    return base + TcSmem::stage + st * kStageBytes + c * kHalf;
+}
+__device__ __forceinline__ unsigned char* stage_v(unsigned char* base, int st, int c) {
+    return base + TcSmem::stage + st * kStageBytes + 2 * kHalf + c * kHalf;
+}
+
+// Byte offset of bf16 element (row, k) of a K-major 128-byte-swizzled tile whose
+// 64-element column blocks are `block_bytes` apart.
+__device__ __forceinline__ uint32_t sw_elem(int row, int k, int block_bytes) {
+    const int chunk = (k & 63) >> 3;
+    return (uint32_t)((k >> 6) * block_bytes + (row >> 3) * 1024 + (row & 7) * 128 +
+                      ((chunk ^ (row & 7)) << 4) + (k & 7) * 2);
+}
+
+__device__ __forceinline__ bool tc_len_ok(int len, const TcParams& p) {
+    return len >= 1 && len <= p.max_seq_len && (int64_t)len <= (int64_t)p.M * p.P;
+}
+
+// 32 consecutive fp32 TMEM columns / 16 of them, this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) { tc::ld_32cols(taddr, v); }
+
+template <int G>
+__global__ void __launch_bounds__(192, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
+    constexpr int HQ = kHeads * G;                 // query heads (MMA N)
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TcSmem::bars);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kStages;
+    uint64_t* s_full = bars + 2 * kStages;
+    uint64_t* s_free = s_full + 2;
+    uint64_t* p_full = s_free + 2;
+    uint64_t* o_full = p_full + 2;
+    uint64_t* o_free = o_full + 2;
+    uint64_t* q_free = o_free + 2;
+    TcMeta* meta = reinterpret_cast<TcMeta*>(smem + TcSmem::meta);
+    float* alpha_buf = reinterpret_cast<float*>(smem + TcSmem::alpha);
+    float* l_buf = reinterpret_cast<float*>(smem + TcSmem::lbuf);
+    float* m_buf = reinterpret_cast<float*>(smem + TcSmem::mbuf);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::tmem_slot);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 1) {
+        tc::alloc(tmem_slot, 128);
+        tc::relinquish();
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 4);
+            mbar_init(&q_free[i], 1);
+        }
+        fence_mbar_init();
+    }
+    // P^T is block-diagonal: zero both buffers once; only diagonal entries are rewritten.
+    for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(smem + TcSmem::pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    // TMEM columns: S buffers [0,32) [32,64); O buffers [64,96) [96,128)
+
+    if (warp == 0) {
+        // ============================ producer ==================================
+        const uint64_t pol = l2_policy_evict_first();
+        int t = 0, k = 0;          // tiles and items issued
+        int b = 0, len = 0, nsp = -1;
+        int64_t cum = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; ok; item += gridDim.x) {
+            while (b < p.B) {
+                if (nsp < 0) {
+                    len = __ldg(p.seq_lens + b);
+                    if (tc_len_ok(len, p)) {
+                        nsp = (len + kSpanTc - 1) / kSpanTc;
+                    } else {
+                        nsp = 0;
+                        if (lane == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
+                    }
+                }
+                if (item < cum + nsp) break;
+                cum += nsp;
+                ++b;
+                nsp = -1;
+            }
+            if (b >= p.B) break;
+            const int split = (int)(item - cum);
+            const int s0 = split * kSpanTc;
+            const int s1 = min(len, s0 + kSpanTc);
+            const int ntiles = (s1 - s0 + kPosT - 1) / kPosT;
+            const int qb = k & 1;
+            if (k >= 2 && !mbar_wait(&q_free[qb], ((k >> 1) - 1) & 1)) {
+                if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+                ok = false;
+                break;
+            }
+            for (int j = 0; j < ntiles; ++j, ++t) {
+                const int st = t % kStages;
+                if (t >= kStages && !mbar_wait(&empty[st], ((t / kStages) - 1) & 1)) {
+                    if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const int p0 = s0 + j * kPosT;
+                const int nvalid = min(kPosT, s1 - p0);
+                const int blk = __ldg(p.block_tables + (int64_t)b * p.M + p0 / p.P);
+                const bool okb = (unsigned)blk < (unsigned)p.N;
+                const uint32_t bytes = (okb ? (uint32_t)kStageBytes : 0u) + (j == 0 ? 2u * HQ * 128u : 0u);
+                if (lane == 0) {
+                    if (!okb) report(p.dev_status, WF_DEV_BAD_BLOCK);
+                    TcMeta m;
+                    m.b = b; m.split = split; m.nsplit = nsp; m.p0 = p0; m.nvalid = nvalid;
+                    m.first = (j == 0); m.last = (j == ntiles - 1); m.item = k;
+                    meta[st] = m;
+                    mbar_arrive_expect_tx(&full[st], bytes);
+                }
+                __syncwarp();
+                const int slot = blk * p.P + p0 % p.P;
+                if (okb && lane < 4) {
+                    const CUtensorMap* tm = lane < 2 ? &tm_k : &tm_v;
+                    unsigned char* dst = lane < 2 ? stage_k(smem, st, lane & 1) : stage_v(smem, st, lane & 1);
+                    tma_load_3d(dst, tm, (lane & 1) * 64, slot, 0, &full[st], pol);
+                }
+                if (j == 0 && (lane == 4 || lane == 5)) {
+                    tma_load_2d(smem + TcSmem::qbuf + qb * kQBytes + (lane - 4) * kQHalf, &tm_q, (lane - 4) * 64,
+                                b * p.H_q, &full[st]);
+                }
+            }
+            ++k;
+        }
+        if (ok) {
+            const int st = t % kStages;
+            if (t < kStages || mbar_wait(&empty[st], ((t / kStages) - 1) & 1)) {
+                if (lane == 0) {
+                    meta[st].nvalid = kEndTile;
+                    mbar_arrive_expect_tx(&full[st], 0);
+                }
+            } else if (lane == 0) {
+                report(p.dev_status, WF_DEV_TIMEOUT);
+            }
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer ================================
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_bf16_f32(kRows, HQ < 16 ? 16 : HQ, 0, 0);
+            constexpr uint32_t idO = tc::idesc_bf16_f32(kD, HQ < 16 ? 16 : HQ, 1, 0);
+            auto issue_pv = [&](int u) {
+                const int su = u % kStages, ub = u & 1;
+                if (!mbar_wait(&p_full[ub], (u >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (u >= 2 && !mbar_wait(&o_free[ub], ((u >> 1) - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                tc::fence_after_sync();
+                const uint32_t vbase = smem_u32(stage_v(smem, su, 0));
+                const uint32_t pb = smem_u32(smem + TcSmem::pbuf + ub * kPBytes);
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk) {
+                    const uint64_t ad = tc::sdesc_sw128(vbase + kk * 2048, kHalf, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(pb + (kk >> 2) * kPHalf + (kk & 3) * 32, 16, 1024);
+                    tc::mma_f16(tmem + 64 + ub * 32, ad, bd, idO, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&o_full[ub]);
+                tc::commit(&empty[su]);
+            };
+            int t = 0;
+            for (;; ++t) {
+                const int st = t % kStages;
+                if (!mbar_wait(&full[st], (t / kStages) & 1)) {
+                    report(p.dev_status, WF_DEV_TIMEOUT);
+                    break;
+                }
+                const TcMeta m = meta[st];
+                if (m.nvalid == kEndTile) break;
+                const int sb = t & 1;
+                if (t >= 2 && !mbar_wait(&s_free[sb], ((t >> 1) - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                tc::fence_after_sync();
+                const uint32_t kbase = smem_u32(stage_k(smem, st, 0));
+                const uint32_t qbase = smem_u32(smem + TcSmem::qbuf + (m.item & 1) * kQBytes);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t ad = tc::sdesc_sw128(kbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+                    tc::mma_f16(tmem + sb * 32, ad, bd, idS, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&s_full[sb]);
+                if (m.last) tc::commit(&q_free[m.item & 1]);
+                if (t >= 1) issue_pv(t - 1);
+            }
+            if (t >= 1) issue_pv(t - 1);
+        }
+    } else {
+        // ==================== accumulate / softmax warps ===========================
+        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const int i = quad * 32 + lane;            // row (softmax) / head dim (accumulate)
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        const int hk = i >> 4;                     // KV head of row i
+        const int pos = i & 15;                    // position of row i within the tile
+        const int upper = lane >> 4;               // which of the warp's two heads
+        float acc[kNq];                            // O^T row d = i, all query heads
+#pragma unroll
+        for (int c = 0; c < kNq; ++c) acc[c] = 0.f;
+        float m_run[G], l_part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m_run[g] = -INFINITY;
+            l_part[g] = 0.f;
+        }
+        TcMeta prev;
+        bool have_prev = false;
+
+        auto accumulate = [&](int u, const TcMeta& m) {
+            const int ub = u & 1;
+            if (!mbar_wait(&o_full[ub], (u >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            tc::fence_after_sync();
+            float o[32];
+            tmem_ld32(tmem + lane_addr + 64 + ub * 32, o);
+            tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[ub]);
+            const float* al = alpha_buf + ub * kNq;
+#pragma unroll
+            for (int c = 0; c < HQ; c += 4) {
+                const float4 a4 = ld_shared_f4(al + c);
+                acc[c] = acc[c] * a4.x + o[c];
+                acc[c + 1] = acc[c + 1] * a4.y + o[c + 1];
+                acc[c + 2] = acc[c + 2] * a4.z + o[c + 2];
+                acc[c + 3] = acc[c + 3] * a4.w + o[c + 3];
+            }
+            if (m.last) {
+                const float* L = l_buf + (m.item & 1) * kNq;
+                const float* Mx = m_buf + (m.item & 1) * kNq;
+                if (m.nsplit == 1) {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (int64_t)m.b * p.H_q * kD + i;
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) dst[c * kD] = __float2bfloat16_rn(acc[c] / L[c]);
+                } else {
+                    const int64_t base = ((int64_t)m.b * p.max_splits + m.split) * p.H_q;
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) p.ws_o[(base + c) * kD + i] = acc[c];
+                    if (i < HQ) p.ws_ml[base + i] = make_float2(Mx[i], L[i]);
+                }
+            }
+        };
+
+        int t = 0;
+        for (;; ++t) {
+            const int st = t % kStages;
+            if (!mbar_wait(&full[st], (t / kStages) & 1)) {
+                report(p.dev_status, WF_DEV_TIMEOUT);
+                break;
+            }
+            const TcMeta m = meta[st];
+            if (m.nvalid == kEndTile) break;
+            // (a) fold in the previous tile's P.V (reads alpha written before the last barrier)
+            if (have_prev) accumulate(t - 1, prev);
+
+            // (b) softmax of this tile
+            const int sb = t & 1;
+            if (!mbar_wait(&s_full[sb], (t >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            tc::fence_after_sync();
+            // this warp's two KV heads' query-head columns [2G*quad, 2G*quad + 2G), width-aligned
+            float sv[2 * G];
+            if constexpr (G == 4) {
+                tc::ld_8cols(tmem + lane_addr + sb * 32 + quad * 8, sv);
+            } else {
+                tc::ld_4cols(tmem + lane_addr + sb * 32 + quad * 4, sv);
+            }
+            tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[sb]);
+            if (m.first) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    m_run[g] = -INFINITY;
+                    l_part[g] = 0.f;
+                }
+            }
+            const bool live = pos < m.nvalid;
+            float al[G];
+            unsigned char* pb = smem + TcSmem::pbuf + sb * kPBytes;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float raw = upper ? sv[G + g] : sv[g];
+                const float s = live ? raw * p.scale_log2 : -INFINITY;
+                float mx = s;
+#pragma unroll
+                for (int mask = 8; mask >= 1; mask >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
+                const float m_new = fmaxf(m_run[g], mx);
+                al[g] = exp2f(m_run[g] - m_new);       // 0 on an item's first tile
+                const __nv_bfloat16 eb = __float2bfloat16_rn(exp2f(s - m_new));
+                l_part[g] = l_part[g] * al[g] + __bfloat162float(eb);
+                m_run[g] = m_new;
+                *reinterpret_cast<__nv_bfloat16*>(pb + sw_elem(hk * G + g, i, kPHalf)) = eb;
+            }
+            if (pos == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) alpha_buf[sb * kNq + hk * G + g] = al[g];
+            }
+            if (m.last) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float x = l_part[g];
+#pragma unroll
+                    for (int mask = 8; mask >= 1; mask >>= 1) x += __shfl_xor_sync(0xffffffffu, x, mask);
+                    if (pos == 0) {
+                        l_buf[(m.item & 1) * kNq + hk * G + g] = x;
+                        m_buf[(m.item & 1) * kNq + hk * G + g] = m_run[g];
+                    }
+                }
+            }
+            if (!live) {
+                // rows past the sequence end: zero V so their 0-weights cannot meet NaN/Inf
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint4* row = reinterpret_cast<uint4*>(stage_v(smem, st, c) + (i >> 3) * 1024 + (i & 7) * 128);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            tc::fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+            prev = m;
+            have_prev = true;
+        }
+        if (have_prev) accumulate(t - 1, prev);
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::dealloc(tmem, 128);
+    }
+}
+
+}  // namespace
+
+bool decode_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
+    const int G = pool.num_kv_heads > 0 ? num_q_heads / pool.num_kv_heads : 0;
+    return pool.dtype == WF_DTYPE_BF16 && pool.head_dim == kD && pool.block_size % kPosT == 0 &&
+           pool.num_kv_heads == kHeads && num_q_heads % pool.num_kv_heads == 0 && (G == 2 || G == 4);
+}
+
+int decode_tc_span() { return kSpanTc; }
+
+cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                                   int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
+                                   float2* ws_ml, int32_t max_splits, uint32_t* dev_status,
+                                   cudaStream_t stream) {
+    const int G = num_q_heads / pool.num_kv_heads;
+    CUtensorMap tm_k, tm_v, tm_q;
+    const uint64_t slots = (uint64_t)pool.num_blocks * pool.block_size;
+    {
+        // (d, slot, head): one box = 16 slots x 8 heads x 64 d, head-major in shared memory
+        const uint64_t dims[3] = {(uint64_t)kD, slots, (uint64_t)kHeads};
+        const uint64_t strides[2] = {(uint64_t)kHeads * kD * 2, (uint64_t)kD * 2};
+        const uint32_t box[3] = {64, (uint32_t)kPosT, (uint32_t)kHeads};
+        cudaError_t e = encode_tiled_bf16(&tm_k, const_cast<void*>(k_pool), 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+        e = encode_tiled_bf16(&tm_v, const_cast<void*>(v_pool), 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)B * num_q_heads};
+        const uint64_t strides[1] = {(uint64_t)kD * 2};
+        const uint32_t box[2] = {64, (uint32_t)num_q_heads};
+        cudaError_t e = encode_tiled_bf16(&tm_q, const_cast<void*>(q), 2, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    TcParams p;
+    p.out = out;
+    p.ws_o = ws_o;
+    p.ws_ml = ws_ml;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.dev_status = dev_status;
+    p.M = max_blocks_per_seq;
+    p.B = B;
+    p.max_seq_len = max_seq_len;
+    p.H_q = num_q_heads;
+    p.H_kv = pool.num_kv_heads;
+    p.G = G;
+    p.N = pool.num_blocks;
+    p.P = pool.block_size;
+    p.max_splits = max_splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int smem = TcSmem::total + 1024;
+    const int64_t items = (int64_t)B * max_splits;
+    const int grid = (int)(items < num_sms() ? items : num_sms());
+    cudaError_t err;
+    if (G == 4) {
+        err = allow_dynamic_smem((const void*)paged_decode_tc_kernel<4>, smem);
+        if (err != cudaSuccess) return err;
+        paged_decode_tc_kernel<4><<<grid, 192, smem, stream>>>(tm_k, tm_v, tm_q, p);
+    } else {
+        err = allow_dynamic_smem((const void*)paged_decode_tc_kernel<2>, smem);
+        if (err != cudaSuccess) return err;
+        paged_decode_tc_kernel<2><<<grid, 192, smem, stream>>>(tm_k, tm_v, tm_q, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace wf

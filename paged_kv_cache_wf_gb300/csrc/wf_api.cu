@@ -1,5 +1,7 @@
 // wf_api.cu -- the extern "C" boundary of libwf: argument validation (before any
 // launch), status mapping, and dispatch to the kernels' launchers.
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -39,6 +41,35 @@ cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
     }
     done[key] = bytes;
     return cudaSuccess;
+}
+
+cudaError_t encode_tiled_bf16(CUtensorMap* map, void* base, int rank, const uint64_t* dims,
+                              const uint64_t* strides, const uint32_t* box) {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (fn == nullptr) {
+            void* f = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || f == nullptr) return cudaErrorNotSupported;
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        }
+    }
+    cuuint64_t d[5];
+    cuuint64_t s[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) s[i] = strides[i];
+    }
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, base, d, s, bx, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace wf

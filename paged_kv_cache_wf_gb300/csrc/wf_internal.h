@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/wf.h"
@@ -18,6 +19,11 @@ int num_sms();
 
 // Opt a kernel into `bytes` of dynamic shared memory (idempotent, cached).
 cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
+
+// Encode a tiled TMA descriptor for a bf16 tensor (128-byte swizzle, no OOB fill).
+// dims[0] is the contiguous dimension; strides[] are bytes for dims 1..rank-1.
+cudaError_t encode_tiled_bf16(CUtensorMap* map, void* base, int rank, const uint64_t* dims,
+                              const uint64_t* strides, const uint32_t* box);
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                      const int64_t* slot_mapping, int32_t num_tokens,
@@ -46,6 +52,17 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
                                 const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                                 int32_t num_q_heads, float scale, const wf_pool_desc& pool,
                                 void* workspace, uint32_t* dev_status, cudaStream_t stream);
+
+// Tensor-core decode (bf16, D = 128, P % 16 == 0); writes outputs or split
+// partials exactly like the CUDA-core kernel, whose combine kernel finishes it.
+bool decode_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads);
+int decode_tc_span();
+cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                                   int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
+                                   float2* ws_ml, int32_t max_splits, uint32_t* dev_status,
+                                   cudaStream_t stream);
 
 // ---- prefill ----------------------------------------------------------------
 cudaError_t launch_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
