@@ -253,8 +253,6 @@ __global__ void __launch_bounds__(192, 1)
             constexpr uint32_t idO = tc::idesc_bf16_f32(kD, HQ < 16 ? 16 : HQ, 1, 0);
             auto issue_pv = [&](int u) {
                 const int su = u % kStages, ub = u & 1;
-                if (!mbar_wait(&p_full[ub], (u >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
-                if (u >= 2 && !mbar_wait(&o_free[ub], ((u >> 1) - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
                 tc::fence_after_sync();
                 const uint32_t vbase = smem_u32(stage_v(smem, su, 0));
                 const uint32_t pb = smem_u32(smem + TcSmem::pbuf + ub * kPBytes);
@@ -267,31 +265,56 @@ __global__ void __launch_bounds__(192, 1)
                 tc::commit(&o_full[ub]);
                 tc::commit(&empty[su]);
             };
-            int t = 0;
-            for (;; ++t) {
-                const int st = t % kStages;
-                if (!mbar_wait(&full[st], (t / kStages) & 1)) {
-                    report(p.dev_status, WF_DEV_TIMEOUT);
-                    break;
+            // Event loop: issue P.V(tp) as soon as its weights are ready (it frees the
+            // stage), otherwise S(tq) as soon as its tile has landed.
+            int tq = 0, tp = 0;
+            bool end_seen = false;
+            uint32_t idle = 0;
+            while (!(end_seen && tp == tq)) {
+                bool did = false;
+                if (tp < tq) {
+                    const int ub = tp & 1;
+                    if (mbar_test(&p_full[ub], (tp >> 1) & 1) &&
+                        (tp < 2 || mbar_test(&o_free[ub], ((tp >> 1) - 1) & 1))) {
+                        issue_pv(tp);
+                        ++tp;
+                        did = true;
+                    }
                 }
-                const TcMeta m = meta[st];
-                if (m.nvalid == kEndTile) break;
-                const int sb = t & 1;
-                if (t >= 2 && !mbar_wait(&s_free[sb], ((t >> 1) - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
-                tc::fence_after_sync();
-                const uint32_t kbase = smem_u32(stage_k(smem, st, 0));
-                const uint32_t qbase = smem_u32(smem + TcSmem::qbuf + (m.item & 1) * kQBytes);
+                if (!end_seen) {
+                    const int st = tq % kStages;
+                    if (mbar_test(&full[st], (tq / kStages) & 1)) {
+                        const TcMeta m = meta[st];
+                        if (m.nvalid == kEndTile) {
+                            end_seen = true;
+                        } else if (tq < 2 || mbar_test(&s_free[tq & 1], ((tq >> 1) - 1) & 1)) {
+                            const int sb = tq & 1;
+                            tc::fence_after_sync();
+                            const uint32_t kbase = smem_u32(stage_k(smem, st, 0));
+                            const uint32_t qbase = smem_u32(smem + TcSmem::qbuf + (m.item & 1) * kQBytes);
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t ad = tc::sdesc_sw128(kbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = tc::sdesc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-                    tc::mma_f16(tmem + sb * 32, ad, bd, idS, kk > 0 ? 1u : 0u);
+                            for (int kk = 0; kk < kD / 16; ++kk) {
+                                const uint64_t ad = tc::sdesc_sw128(kbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                                const uint64_t bd = tc::sdesc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+                                tc::mma_f16(tmem + sb * 32, ad, bd, idS, kk > 0 ? 1u : 0u);
+                            }
+                            tc::commit(&s_full[sb]);
+                            if (m.last) tc::commit(&q_free[m.item & 1]);
+                            ++tq;
+                            did = true;
+                        }
+                    }
                 }
-                tc::commit(&s_full[sb]);
-                if (m.last) tc::commit(&q_free[m.item & 1]);
-                if (t >= 1) issue_pv(t - 1);
+                if (did) {
+                    idle = 0;
+                } else {
+                    if (++idle > (1u << 24)) {
+                        report(p.dev_status, WF_DEV_TIMEOUT);
+                        break;
+                    }
+                    if (idle > 8) __nanosleep(64);  // leave issue slots to the softmax warp on this SMSP
+                }
             }
-            if (t >= 1) issue_pv(t - 1);
         }
     } else {
         // ==================== accumulate / softmax warps ===========================
