@@ -283,6 +283,12 @@ cudaError_t launch_paged_prefill(void* out, const void* q, const void* k_pool, c
                                  int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
                                  int32_t num_q_heads, float scale, const wf_pool_desc& pool,
                                  uint32_t* dev_status, cudaStream_t stream) {
+    if (prefill_tc_supported(pool, num_q_heads) &&
+        (int64_t)pool.num_blocks * pool.block_size <= INT32_MAX && total_q > 0) {
+        return launch_paged_prefill_tc(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens,
+                                       B, total_q, max_q_len, max_seq_len, num_q_heads, scale, pool, dev_status,
+                                       stream);
+    }
     PrefillParams p;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.q = static_cast<const __nv_bfloat16*>(q);

@@ -1,0 +1,449 @@
+// paged_prefill_tc.cu -- pipelined, warp-specialised causal prefill on tcgen05 for
+// bf16 pools whose block size is a multiple of 16.
+//
+// What is computed (tiny-vllm-py, "KV Cache": prefill attention is causal;
+// "Dense vs. Ragged batching"): query row i of request b (position c_b + i, c_b =
+// seq_lens[b] - n_b) attends to positions 0 .. c_b + i of its KV head, read from the
+// [N, P, H_kv, D] pool through block_table[b][p / P], offset p % P (ember, "The core
+// idea"); query head g uses KV head g / G (weft, "Shapes and symbols").
+//
+// GB300 design.  One CTA = one request, one KV head and 128 rows r = (token, g):
+// 128/G consecutive query tokens times the G query heads that share the KV head, so
+// every K/V tile serves the whole group.
+//   warp 0   producer: TMA loads of the Q tile (3D box d x head x token) and, tile by
+//            tile, of 128 keys of K and V gathered block by block through the table
+//            (16-slot boxes, 128-byte swizzle, several issuing lanes) into a 2-stage ring.
+//   warp 1   MMA issuer, event loop: S(j) = Q K_j^T into one of two TMEM S buffers
+//            (M=128 rows, N=128 keys, K=D) as soon as tile j has landed, and
+//            O += P(j) V_j (M=128, N=D, K=128 keys, V read MN-major) as soon as the
+//            softmax has written P(j); commits release stages and buffers.
+//   warps 2-5  softmax, thread r <-> row r <-> TMEM lane r: causal mask (only on
+//            tiles that cross the diagonal), online softmax in the exp2 domain with a
+//            lazy rescale (O in TMEM is rescaled only when a row max grows by more than
+//            2^8, so almost never), P written as bf16 into a swizzled shared tile; the
+//            epilogue divides O by the row sum.
+#include <cuda.h>
+
+#include "wf_internal.h"
+
+namespace wf {
+
+namespace {
+
+constexpr int PM = 128;          // rows per CTA
+constexpr int PN = 128;          // keys per tile
+constexpr int kPfStages = 2;
+constexpr float kLazy = 8.f;     // rescale O only when the row max grows by more than 2^8
+
+struct PfParams {
+    __nv_bfloat16* out;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* cu_q_lens;
+    uint32_t* dev_status;
+    int32_t M, B, total_q, max_q_len, max_seq_len, H_q, H_kv, G, N, P, nqblk;
+    float scale_log2;
+};
+
+template <int D, int G>
+struct PfLayout {
+    static constexpr int BMQ = PM / G;              // query tokens per CTA
+    static constexpr int NC = D / 64;               // 64-wide column blocks of D
+    static constexpr int QBYTES = PM * D * 2;
+    static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile
+    static constexpr int STAGE = 2 * NC * KVHALF;   // K then V
+    static constexpr int PHALF = PM * 128;          // one 64-key column block of P
+    static constexpr int PBYTES = PM * PN * 2;
+    static constexpr int q = 0;
+    static constexpr int kv = QBYTES;
+    static constexpr int pbuf = kv + kPfStages * STAGE;
+    static constexpr int bars = pbuf + 2 * PBYTES;
+    // q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], pv_done[2]
+    static constexpr int nbars = 1 + 6 * 2;
+    static constexpr int tmem_slot = bars + nbars * 8;
+    static constexpr int total = tmem_slot + 16;
+    static constexpr int TMEM_COLS = 512;           // S0 [0,128) S1 [128,256) O [256, 256+D)
+    static_assert(total + 1024 <= 232448, "prefill tile exceeds shared memory");
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(192, 1)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
+    using L = PfLayout<D, G>;
+    const int qb = p.nqblk - 1 - (int)blockIdx.x;   // the longest query blocks start first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int q_begin = __ldg(p.cu_q_lens + b);
+    const int q_end = __ldg(p.cu_q_lens + b + 1);
+    const int n = q_end - q_begin;
+    const int len = __ldg(p.seq_lens + b);
+    const bool bad = q_begin < 0 || n < 0 || q_end > p.total_q || n > p.max_q_len || len < n ||
+                     len > p.max_seq_len || (int64_t)len > (int64_t)p.M * p.P;
+    if (bad) {
+        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
+        return;
+    }
+    const int i0 = qb * L::BMQ;
+    if (i0 >= n) return;
+    const int c = len - n;                            // cached prefix
+    const int rows_tok = min(L::BMQ, n - i0);
+    const int kend = c + i0 + rows_tok;               // keys this CTA needs: [0, kend)
+    const int ntiles = (kend + PN - 1) / PN;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + 2;
+    uint64_t* s_full = kv_empty + 2;
+    uint64_t* s_free = s_full + 2;
+    uint64_t* p_full = s_free + 2;
+    uint64_t* pv_done = p_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
+    auto k_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + cb * L::KVHALF; };
+    auto v_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + (L::NC + cb) * L::KVHALF; };
+
+    if (warp == 1) {
+        tc::alloc(tmem_slot, L::TMEM_COLS);
+        tc::relinquish();
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+        }
+        fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ============================= producer =====================================
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, (uint32_t)L::QBYTES);
+#pragma unroll
+            for (int cb = 0; cb < L::NC; ++cb)
+                tma_load_3d_nohint(smem + L::q + cb * (PM * 128), &tm_q, cb * 64, h * G, q_begin + i0, q_full);
+        }
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            if (j >= 2 && !mbar_wait(&kv_empty[st], ((j >> 1) - 1) & 1)) {
+                if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+                break;
+            }
+            const int k0 = j * PN;
+            const int kt = min(PN, kend - k0);
+            const int nbox = (kt + 15) >> 4;
+            int blk = 0;
+            bool okb = false;
+            if (lane < nbox) {
+                const int pos = k0 + lane * 16;
+                blk = __ldg(p.block_tables + (int64_t)b * p.M + pos / p.P);
+                okb = (unsigned)blk < (unsigned)p.N;
+                if (!okb) report(p.dev_status, WF_DEV_BAD_BLOCK);
+            }
+            const unsigned okm = __ballot_sync(0xffffffffu, okb);
+            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)__popc(okm) * 2u * L::NC * 2048u);
+            __syncwarp();
+            if (okb) {
+                const int slot = blk * p.P + (k0 + lane * 16) % p.P;
+#pragma unroll
+                for (int cb = 0; cb < L::NC; ++cb) {
+                    tma_load_3d_nohint(k_tile(st, cb) + lane * 2048, &tm_k, cb * 64, slot, h, &kv_full[st]);
+                    tma_load_3d_nohint(v_tile(st, cb) + lane * 2048, &tm_v, cb * 64, slot, h, &kv_full[st]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ============================= MMA issuer ===================================
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
+            constexpr uint32_t idO = tc::idesc_bf16_f32(PM, D, 0, 1);
+            bool ok = mbar_wait(q_full, 0);
+            if (!ok) report(p.dev_status, WF_DEV_TIMEOUT);
+            const uint32_t qbase = smem_u32(smem + L::q);
+            int tq = 0, tp = 0;
+            uint32_t idle = 0;
+            while (ok && tp < ntiles) {
+                bool did = false;
+                if (tp < tq) {
+                    const int pb = tp & 1;
+                    if (mbar_test(&p_full[pb], (tp >> 1) & 1)) {
+                        tc::fence_after_sync();
+                        const uint32_t pbase = smem_u32(smem + L::pbuf + pb * L::PBYTES);
+                        const uint32_t vbase = smem_u32(v_tile(tp & 1, 0));
+#pragma unroll
+                        for (int kk = 0; kk < PN / 16; ++kk) {
+                            const uint64_t ad = tc::sdesc_sw128(pbase + (kk >> 2) * L::PHALF + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2048, L::KVHALF, 1024);
+                            tc::mma_f16(tmem + 256, ad, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc::commit(&pv_done[pb]);
+                        tc::commit(&kv_empty[tp & 1]);
+                        ++tp;
+                        did = true;
+                    }
+                }
+                if (tq < ntiles) {
+                    const int st = tq & 1;
+                    if (mbar_test(&kv_full[st], (tq >> 1) & 1) &&
+                        (tq < 2 || mbar_test(&s_free[st], ((tq >> 1) - 1) & 1))) {
+                        tc::fence_after_sync();
+                        const uint32_t kbase = smem_u32(k_tile(st, 0));
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
+                            const uint32_t koff = (kk >> 2) * L::KVHALF + (kk & 3) * 32;
+                            tc::mma_f16(tmem + st * 128, tc::sdesc_sw128(qbase + off, 16, 1024),
+                                        tc::sdesc_sw128(kbase + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                        }
+                        tc::commit(&s_full[st]);
+                        ++tq;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    idle = 0;
+                } else {
+                    if (++idle > (1u << 24)) {
+                        report(p.dev_status, WF_DEV_TIMEOUT);
+                        break;
+                    }
+                    if (idle > 8) __nanosleep(32);
+                }
+            }
+        }
+    } else {
+        // ============================= softmax ======================================
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                  // row / TMEM lane
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        const int tok = r / G, g = r % G;
+        const int qi = i0 + tok;
+        const bool row_valid = qi < n;
+        const int last_key = c + qi;                     // row sees keys 0 .. last_key
+        float m_ref = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int sb = j & 1;
+            const int k0 = j * PN;
+            if (!mbar_wait(&s_full[sb], (j >> 1) & 1)) {
+                report(p.dev_status, WF_DEV_TIMEOUT);
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            float s[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) tc::ld_32cols(tmem + lane_addr + sb * 128 + c4 * 32, s[c4]);
+            tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[sb]);
+
+            // keys of this tile that some row of the CTA may not see: mask them
+            const bool masked = (k0 + PN - 1 > c + i0) || !row_valid;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float x = s[c4][e] * p.scale_log2;
+                    if (masked) x = (row_valid && k0 + c4 * 32 + e <= last_key) ? x : -INFINITY;
+                    s[c4][e] = x;
+                    mt = fmaxf(mt, x);
+                }
+            // lazy online softmax: move the reference max only when it grows by > 2^8
+            float alpha = 1.f;
+            if (j == 0) {
+                m_ref = (mt == -INFINITY) ? 0.f : mt;
+            } else if (mt > m_ref + kLazy) {
+                alpha = exp2f(m_ref - mt);
+                m_ref = mt;
+            }
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                // O must hold P.V of tile j-1 before it is rescaled
+                if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                tc::fence_after_sync();
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    float o[32];
+                    tc::ld_32cols(tmem + lane_addr + 256 + c4 * 32, o);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tc::st_32cols(tmem + lane_addr + 256 + c4 * 32, o);
+                }
+                tc::wait_st();
+            }
+            l_run *= alpha;
+            // P buffer sb was last read by P.V of tile j-2
+            if (j >= 2 && !mbar_wait(&pv_done[sb], ((j - 2) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            unsigned char* pt = smem + L::pbuf + sb * L::PBYTES;
+            float psum = 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                for (int e8 = 0; e8 < 4; ++e8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float a = exp2f(s[c4][e8 * 8 + 2 * u] - m_ref);
+                        const float bb = exp2f(s[c4][e8 * 8 + 2 * u + 1] - m_ref);
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, bb);
+                        const float2 back = __bfloat1622float2(h2);
+                        psum += back.x + back.y;
+                        w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    const int chunk = c4 * 4 + e8;  // 8-key chunk 0..15
+                    const uint32_t off = (chunk >> 3) * L::PHALF + (r >> 3) * 1024 + (r & 7) * 128 +
+                                         (((chunk & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(pt + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            l_run += psum;
+            // keys past the CTA's end were not loaded (or are stale): zero their V rows
+            if (k0 + r >= kend) {
+#pragma unroll
+                for (int cb = 0; cb < L::NC; ++cb) {
+                    uint4* row = reinterpret_cast<uint4*>(v_tile(sb, cb) + (r >> 3) * 1024 + (r & 7) * 128);
+#pragma unroll
+                    for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+        }
+        // ---- epilogue: O / l -> bf16 ---------------------------------------------
+        if (ok) {
+            const int last = ntiles - 1;
+            if (!mbar_wait(&pv_done[last & 1], (last >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            tc::fence_after_sync();
+            const float inv = row_valid ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                float o[32];
+                tc::ld_32cols(tmem + lane_addr + 256 + c4 * 32, o);
+                tc::wait_ld();
+                if (row_valid) {
+                    __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + c4 * 32;
+#pragma unroll
+                    for (int e8 = 0; e8 < 4; ++e8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(o[e8 * 8 + 0] * inv, o[e8 * 8 + 1] * inv);
+                        v.y = pack_bf16x2(o[e8 * 8 + 2] * inv, o[e8 * 8 + 3] * inv);
+                        v.z = pack_bf16x2(o[e8 * 8 + 4] * inv, o[e8 * 8 + 5] * inv);
+                        v.w = pack_bf16x2(o[e8 * 8 + 6] * inv, o[e8 * 8 + 7] * inv);
+                        *reinterpret_cast<uint4*>(dst + e8 * 8) = v;
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+template <int D, int G>
+cudaError_t launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, PfParams p,
+                      cudaStream_t stream) {
+    using L = PfLayout<D, G>;
+    p.nqblk = (p.max_q_len + L::BMQ - 1) / L::BMQ;
+    const int smem = L::total + 1024;
+    auto kern = paged_prefill_tc_kernel<D, G>;
+    cudaError_t err = allow_dynamic_smem((const void*)kern, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid(p.nqblk, p.H_kv, p.B);
+    kern<<<grid, 192, smem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
+    if (pool.dtype != WF_DTYPE_BF16 || pool.block_size % 16 != 0) return false;
+    if (pool.head_dim != 64 && pool.head_dim != 128) return false;
+    if (num_q_heads % pool.num_kv_heads != 0) return false;
+    const int G = num_q_heads / pool.num_kv_heads;
+    return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+cudaError_t launch_paged_prefill_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
+                                    int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
+                                    int32_t num_q_heads, float scale, const wf_pool_desc& pool,
+                                    uint32_t* dev_status, cudaStream_t stream) {
+    const int D = pool.head_dim;
+    const int G = num_q_heads / pool.num_kv_heads;
+    CUtensorMap tq, tk, tv;
+    {
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)num_q_heads, (uint64_t)total_q};
+        const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)num_q_heads * D * 2};
+        const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(PM / G)};
+        cudaError_t e = encode_tiled_bf16(&tq, const_cast<void*>(q), 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const uint64_t slots = (uint64_t)pool.num_blocks * pool.block_size;
+        const uint64_t dims[3] = {(uint64_t)D, slots, (uint64_t)pool.num_kv_heads};
+        const uint64_t strides[2] = {(uint64_t)pool.num_kv_heads * D * 2, (uint64_t)D * 2};
+        const uint32_t box[3] = {64, 16, 1};
+        cudaError_t e = encode_tiled_bf16(&tk, const_cast<void*>(k_pool), 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+        e = encode_tiled_bf16(&tv, const_cast<void*>(v_pool), 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    PfParams p;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.cu_q_lens = cu_q_lens;
+    p.dev_status = dev_status;
+    p.M = max_blocks_per_seq;
+    p.B = B;
+    p.total_q = total_q;
+    p.max_q_len = max_q_len;
+    p.max_seq_len = max_seq_len;
+    p.H_q = num_q_heads;
+    p.H_kv = pool.num_kv_heads;
+    p.G = G;
+    p.N = pool.num_blocks;
+    p.P = pool.block_size;
+    p.nqblk = 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    if (D == 128) {
+        switch (G) {
+            case 1: return launch_pf<128, 1>(tq, tk, tv, p, stream);
+            case 2: return launch_pf<128, 2>(tq, tk, tv, p, stream);
+            case 4: return launch_pf<128, 4>(tq, tk, tv, p, stream);
+            default: return launch_pf<128, 8>(tq, tk, tv, p, stream);
+        }
+    }
+    switch (G) {
+        case 1: return launch_pf<64, 1>(tq, tk, tv, p, stream);
+        case 2: return launch_pf<64, 2>(tq, tk, tv, p, stream);
+        case 4: return launch_pf<64, 4>(tq, tk, tv, p, stream);
+        default: return launch_pf<64, 8>(tq, tk, tv, p, stream);
+    }
+}
+
+}  // namespace wf

@@ -373,6 +373,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0,
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_nohint(void* dst, const void* tmap, int c0, int c1, int c2,
+                                                   uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"

@@ -64,7 +64,16 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
                                    float2* ws_ml, int32_t max_splits, uint32_t* dev_status,
                                    cudaStream_t stream);
 
-// ---- prefill ----------------------------------------------------------------
+// ---- prefill ------------------------------------------------------------------
+// Pipelined tcgen05 prefill (bf16, P % 16 == 0, G in {1, 2, 4, 8}, D in {64, 128}).
+bool prefill_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads);
+cudaError_t launch_paged_prefill_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
+                                    int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
+                                    int32_t num_q_heads, float scale, const wf_pool_desc& pool,
+                                    uint32_t* dev_status, cudaStream_t stream);
+
 cudaError_t launch_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
                                  const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
