@@ -144,25 +144,24 @@ __global__ void __launch_bounds__(192, 1)
             }
             const int k0 = j * PN;
             const int kt = min(PN, kend - k0);
-            const int nbox = (kt + 15) >> 4;
-            int blk = 0;
+            const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile
+            // one 2 KB box per lane: lane = (K or V, column block, 16-key block)
+            const int bx = lane & 7, cb = (lane >> 3) & 1, isv = lane >> 4;
             bool okb = false;
-            if (lane < nbox) {
-                const int pos = k0 + lane * 16;
+            int blk = 0;
+            if (bx < nbox && cb < L::NC) {
+                const int pos = k0 + bx * 16;
                 blk = __ldg(p.block_tables + (int64_t)b * p.M + pos / p.P);
                 okb = (unsigned)blk < (unsigned)p.N;
-                if (!okb) report(p.dev_status, WF_DEV_BAD_BLOCK);
+                if (!okb && cb == 0 && isv == 0) report(p.dev_status, WF_DEV_BAD_BLOCK);
             }
             const unsigned okm = __ballot_sync(0xffffffffu, okb);
-            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)__popc(okm) * 2u * L::NC * 2048u);
+            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)__popc(okm) * 2048u);
             __syncwarp();
             if (okb) {
-                const int slot = blk * p.P + (k0 + lane * 16) % p.P;
-#pragma unroll
-                for (int cb = 0; cb < L::NC; ++cb) {
-                    tma_load_3d_nohint(k_tile(st, cb) + lane * 2048, &tm_k, cb * 64, slot, h, &kv_full[st]);
-                    tma_load_3d_nohint(v_tile(st, cb) + lane * 2048, &tm_v, cb * 64, slot, h, &kv_full[st]);
-                }
+                const int slot = blk * p.P + (k0 + bx * 16) % p.P;
+                unsigned char* dst = (isv ? v_tile(st, cb) : k_tile(st, cb)) + bx * 2048;
+                tma_load_3d_nohint(dst, isv ? &tm_v : &tm_k, cb * 64, slot, h, &kv_full[st]);
             }
         }
     } else if (warp == 1) {
@@ -252,24 +251,32 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[sb]);
 
-            // keys of this tile that some row of the CTA may not see: mask them
+            // keys of this tile that some row of the CTA may not see: mask them.
+            // The row max is taken on raw scores (scale > 0) and scaled once.
             const bool masked = (k0 + PN - 1 > c + i0) || !row_valid;
-            float mt = -INFINITY;
+            float mraw = -INFINITY;
+            if (masked) {
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
+                for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float x = s[c4][e] * p.scale_log2;
-                    if (masked) x = (row_valid && k0 + c4 * 32 + e <= last_key) ? x : -INFINITY;
-                    s[c4][e] = x;
-                    mt = fmaxf(mt, x);
-                }
+                    for (int e = 0; e < 32; ++e) {
+                        const bool vis = row_valid && k0 + c4 * 32 + e <= last_key;
+                        s[c4][e] = vis ? s[c4][e] : -INFINITY;
+                        mraw = fmaxf(mraw, s[c4][e]);
+                    }
+            } else {
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mraw = fmaxf(mraw, s[c4][e]);
+            }
+            const float mt = mraw * p.scale_log2;
             // lazy online softmax: move the reference max only when it grows by > 2^8
             float alpha = 1.f;
             if (j == 0) {
                 m_ref = (mt == -INFINITY) ? 0.f : mt;
             } else if (mt > m_ref + kLazy) {
-                alpha = exp2f(m_ref - mt);
+                alpha = ex2(m_ref - mt);
                 m_ref = mt;
             }
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -291,7 +298,9 @@ __global__ void __launch_bounds__(192, 1)
             // P buffer sb was last read by P.V of tile j-2
             if (j >= 2 && !mbar_wait(&pv_done[sb], ((j - 2) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             unsigned char* pt = smem + L::pbuf + sb * L::PBYTES;
-            float psum = 0.f;
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 psum2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
@@ -299,19 +308,18 @@ __global__ void __launch_bounds__(192, 1)
                     uint32_t w[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const float a = exp2f(s[c4][e8 * 8 + 2 * u] - m_ref);
-                        const float bb = exp2f(s[c4][e8 * 8 + 2 * u + 1] - m_ref);
-                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, bb);
-                        const float2 back = __bfloat1622float2(h2);
-                        psum += back.x + back.y;
-                        w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+                        // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
+                        const float2 x = __ffma2_rn(make_float2(s[c4][e8 * 8 + 2 * u], s[c4][e8 * 8 + 2 * u + 1]), sc2, nm2);
+                        const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
+                        psum2 = __fadd2_rn(psum2, e2);
+                        w[u] = pack_bf16x2(e2.x, e2.y);
                     }
                     const int chunk = c4 * 4 + e8;  // 8-key chunk 0..15
                     const uint32_t off = (chunk >> 3) * L::PHALF + (r >> 3) * 1024 + (r & 7) * 128 +
                                          (((chunk & 7) ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4*>(pt + off) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-            l_run += psum;
+            l_run += psum2.x + psum2.y;
             // keys past the CTA's end were not loaded (or are stale): zero their V rows
             if (k0 + r >= kend) {
 #pragma unroll

@@ -55,6 +55,13 @@ __device__ __forceinline__ void widen_chunk<BF16>(const uint4& c, float* f) {
     f[4] = d.x; f[5] = d.y; f[6] = e.x; f[7] = e.y;
 }
 
+// 2^x on the SFU (approximate, flushes denormals); 2^-inf = +0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Store n (1, 2 or 4) fp32 values as the storage type at p (naturally aligned).
 template <typename E, int n>
 __device__ __forceinline__ void store_out(void* p, const float* f);
