@@ -58,16 +58,16 @@ struct PfLayout {
     static constexpr int kv = QBYTES;
     static constexpr int pbuf = kv + kPfStages * STAGE;
     static constexpr int bars = pbuf + 2 * PBYTES;
-    // q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], pv_done[2]
-    static constexpr int nbars = 1 + 6 * 2;
+    // q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[half][2], pv_done[half][2]
+    static constexpr int nbars = 1 + 4 * 2 + 2 * 4;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
-    static constexpr int TMEM_COLS = 512;           // S0 [0,128) S1 [128,256) O [256, 256+D)
+    static constexpr int TMEM_COLS = 512;           // S0 [0,128) S1 [128,256) O_0, O_1 from 256
     static_assert(total + 1024 <= 232448, "prefill tile exceeds shared memory");
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
     using L = PfLayout<D, G>;
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* kv_empty = kv_full + 2;
     uint64_t* s_full = kv_empty + 2;
     uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;
-    uint64_t* pv_done = p_full + 2;
+    uint64_t* p_full = s_free + 2;    // [half][parity]
+    uint64_t* pv_done = p_full + 4;   // [half][parity]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     auto k_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + cb * L::KVHALF; };
     auto v_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + (L::NC + cb) * L::KVHALF; };
@@ -117,7 +117,9 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
+            mbar_init(&s_free[i], 8);
+        }
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
         }
@@ -166,31 +168,34 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         // ============================= MMA issuer ===================================
+        // Keys 0-63 and 64-127 of every tile have independent softmax states and
+        // accumulators (half h: O_h += P[:, 64h:64h+64] V[64h:64h+64, :]).
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(PM, D, 0, 1);
             bool ok = mbar_wait(q_full, 0);
             if (!ok) report(p.dev_status, WF_DEV_TIMEOUT);
             const uint32_t qbase = smem_u32(smem + L::q);
-            int tq = 0, tp = 0;
+            int tq = 0, tp[2] = {0, 0};
             uint32_t idle = 0;
-            while (ok && tp < ntiles) {
+            while (ok && (tp[0] < ntiles || tp[1] < ntiles)) {
                 bool did = false;
-                if (tp < tq) {
-                    const int pb = tp & 1;
-                    if (mbar_test(&p_full[pb], (tp >> 1) & 1)) {
-                        tc::fence_after_sync();
-                        const uint32_t pbase = smem_u32(smem + L::pbuf + pb * L::PBYTES);
-                        const uint32_t vbase = smem_u32(v_tile(tp & 1, 0));
 #pragma unroll
-                        for (int kk = 0; kk < PN / 16; ++kk) {
-                            const uint64_t ad = tc::sdesc_sw128(pbase + (kk >> 2) * L::PHALF + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2048, L::KVHALF, 1024);
-                            tc::mma_f16(tmem + 256, ad, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int u = tp[hh];
+                    if (u < tq && mbar_test(&p_full[hh * 2 + (u & 1)], (u >> 1) & 1)) {
+                        tc::fence_after_sync();
+                        const uint32_t pbase = smem_u32(smem + L::pbuf + (u & 1) * L::PBYTES + hh * L::PHALF);
+                        const uint32_t vbase = smem_u32(v_tile(u & 1, 0));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = tc::sdesc_sw128(pbase + kk * 32, 16, 1024);
+                            const uint64_t bd = tc::sdesc_sw128(vbase + (4 * hh + kk) * 2048, L::KVHALF, 1024);
+                            tc::mma_f16(tmem + 256 + hh * D, ad, bd, idO, (u > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc::commit(&pv_done[pb]);
-                        tc::commit(&kv_empty[tp & 1]);
-                        ++tp;
+                        tc::commit(&pv_done[hh * 2 + (u & 1)]);
+                        if (tp[hh ^ 1] > u) tc::commit(&kv_empty[u & 1]);  // both halves read V(u)
+                        tp[hh] = u + 1;
                         did = true;
                     }
                 }
@@ -225,6 +230,8 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ============================= softmax ======================================
+        // warps 2-5: keys 0-63 of each tile (half 0); warps 6-9: keys 64-127 (half 1).
+        const int hh = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                  // row / TMEM lane
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
@@ -232,99 +239,104 @@ __global__ void __launch_bounds__(192, 1)
         const int qi = i0 + tok;
         const bool row_valid = qi < n;
         const int last_key = c + qi;                     // row sees keys 0 .. last_key
+        const uint32_t o_col = 256 + hh * D;             // this half's accumulator
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
             const int sb = j & 1;
-            const int k0 = j * PN;
+            const int k0 = j * PN + hh * 64;             // first key of this half
             if (!mbar_wait(&s_full[sb], (j >> 1) & 1)) {
                 report(p.dev_status, WF_DEV_TIMEOUT);
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            float s[4][32];
+            float s[2][32];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tc::ld_32cols(tmem + lane_addr + sb * 128 + c4 * 32, s[c4]);
+            for (int c2 = 0; c2 < 2; ++c2) tc::ld_32cols(tmem + lane_addr + sb * 128 + hh * 64 + c2 * 32, s[c2]);
             tc::wait_ld();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[sb]);
 
-            // keys of this tile that some row of the CTA may not see: mask them.
-            // The row max is taken on raw scores (scale > 0) and scaled once.
-            const bool masked = (k0 + PN - 1 > c + i0) || !row_valid;
+            // keys some row of the CTA may not see: mask them.  The row max is taken
+            // on raw scores (scale > 0) and scaled once.
+            const bool masked = (k0 + 63 > c + i0) || !row_valid;
             float mraw = -INFINITY;
             if (masked) {
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
+                for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const bool vis = row_valid && k0 + c4 * 32 + e <= last_key;
-                        s[c4][e] = vis ? s[c4][e] : -INFINITY;
-                        mraw = fmaxf(mraw, s[c4][e]);
+                        const bool vis = row_valid && k0 + c2 * 32 + e <= last_key;
+                        s[c2][e] = vis ? s[c2][e] : -INFINITY;
+                        mraw = fmaxf(mraw, s[c2][e]);
                     }
             } else {
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
+                for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mraw = fmaxf(mraw, s[c4][e]);
+                    for (int e = 0; e < 32; ++e) mraw = fmaxf(mraw, s[c2][e]);
             }
             const float mt = mraw * p.scale_log2;
             // lazy online softmax: move the reference max only when it grows by > 2^8
+            // (while nothing has been visible yet, O_h and l are still zero)
             float alpha = 1.f;
-            if (j == 0) {
-                m_ref = (mt == -INFINITY) ? 0.f : mt;
+            if (m_ref == -INFINITY) {
+                m_ref = mt;
             } else if (mt > m_ref + kLazy) {
                 alpha = ex2(m_ref - mt);
                 m_ref = mt;
             }
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                // O must hold P.V of tile j-1 before it is rescaled
-                if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                // O_h must hold P.V of tile j-1 before it is rescaled
+                if (!mbar_wait(&pv_done[hh * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1))
+                    report(p.dev_status, WF_DEV_TIMEOUT);
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     float o[32];
-                    tc::ld_32cols(tmem + lane_addr + 256 + c4 * 32, o);
+                    tc::ld_32cols(tmem + lane_addr + o_col + c4 * 32, o);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tc::st_32cols(tmem + lane_addr + 256 + c4 * 32, o);
+                    tc::st_32cols(tmem + lane_addr + o_col + c4 * 32, o);
                 }
                 tc::wait_st();
             }
             l_run *= alpha;
-            // P buffer sb was last read by P.V of tile j-2
-            if (j >= 2 && !mbar_wait(&pv_done[sb], ((j - 2) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
-            unsigned char* pt = smem + L::pbuf + sb * L::PBYTES;
+            // this half of P buffer sb was last read by P.V of tile j-2
+            if (j >= 2 && !mbar_wait(&pv_done[hh * 2 + sb], ((j - 2) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            unsigned char* pt = smem + L::pbuf + sb * L::PBYTES + hh * L::PHALF;
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            const float2 nm2 = make_float2(-m_use, -m_use);
             float2 psum2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
+            for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
                 for (int e8 = 0; e8 < 4; ++e8) {
                     uint32_t w[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
-                        const float2 x = __ffma2_rn(make_float2(s[c4][e8 * 8 + 2 * u], s[c4][e8 * 8 + 2 * u + 1]), sc2, nm2);
+                        const float2 x = __ffma2_rn(make_float2(s[c2][e8 * 8 + 2 * u], s[c2][e8 * 8 + 2 * u + 1]),
+                                                    sc2, nm2);
                         const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
                         psum2 = __fadd2_rn(psum2, e2);
                         w[u] = pack_bf16x2(e2.x, e2.y);
                     }
-                    const int chunk = c4 * 4 + e8;  // 8-key chunk 0..15
-                    const uint32_t off = (chunk >> 3) * L::PHALF + (r >> 3) * 1024 + (r & 7) * 128 +
-                                         (((chunk & 7) ^ (r & 7)) << 4);
+                    const int chunk = c2 * 4 + e8;  // 8-key chunk within this half
+                    const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4*>(pt + off) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             l_run += psum2.x + psum2.y;
-            // keys past the CTA's end were not loaded (or are stale): zero their V rows
-            if (k0 + r >= kend) {
-#pragma unroll
-                for (int cb = 0; cb < L::NC; ++cb) {
-                    uint4* row = reinterpret_cast<uint4*>(v_tile(sb, cb) + (r >> 3) * 1024 + (r & 7) * 128);
+            // keys past the CTA's end were not loaded (or are stale): zero their V rows.
+            // Thread r of half h owns key 64h + (r % 64) and column block r / 64.
+            {
+                const int key = hh * 64 + (r & 63), cb = r >> 6;
+                if (cb < L::NC && j * PN + key >= kend) {
+                    uint4* row = reinterpret_cast<uint4*>(v_tile(sb, cb) + (key >> 3) * 1024 + (key & 7) * 128);
 #pragma unroll
                     for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -332,28 +344,46 @@ __global__ void __launch_bounds__(192, 1)
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
+            if (lane == 0) mbar_arrive(&p_full[hh * 2 + sb]);
         }
-        // ---- epilogue: O / l -> bf16 ---------------------------------------------
+        // ---- epilogue: merge the two halves, O / l -> bf16 ------------------------------
+        // The Q tile is no longer read (every S MMA has completed): it holds the
+        // (m, l) exchange between the halves.
+        const int last = ntiles - 1;
+        if (ok && !mbar_wait(&pv_done[hh * 2 + (last & 1)], (last >> 1) & 1)) {
+            report(p.dev_status, WF_DEV_TIMEOUT);
+            ok = false;
+        }
+        float2* xch = reinterpret_cast<float2*>(smem + L::q);
+        xch[hh * PM + r] = make_float2(m_ref, l_run);
+        named_bar_sync(1, 256);
         if (ok) {
-            const int last = ntiles - 1;
-            if (!mbar_wait(&pv_done[last & 1], (last >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            const float2 other = xch[(hh ^ 1) * PM + r];
+            const float m0 = hh == 0 ? m_ref : other.x, l0 = hh == 0 ? l_run : other.y;
+            const float m1 = hh == 0 ? other.x : m_ref, l1 = hh == 0 ? other.y : l_run;
+            const float m = fmaxf(m0, m1);
+            const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - m);
+            const float w1 = m1 == -INFINITY ? 0.f : ex2(m1 - m);
+            const float inv = row_valid ? 1.f / (l0 * w0 + l1 * w1) : 0.f;
+            const float a0 = w0 * inv, a1 = w1 * inv;
+            // half h stores columns [h*D/2, (h+1)*D/2)
             tc::fence_after_sync();
-            const float inv = row_valid ? 1.f / l_run : 0.f;
 #pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-                float o[32];
-                tc::ld_32cols(tmem + lane_addr + 256 + c4 * 32, o);
+            for (int c4 = 0; c4 < D / 64; ++c4) {
+                const int col = hh * (D / 2) + c4 * 32;
+                float o0[32], o1[32];
+                tc::ld_32cols(tmem + lane_addr + 256 + col, o0);
+                tc::ld_32cols(tmem + lane_addr + 256 + D + col, o1);
                 tc::wait_ld();
                 if (row_valid) {
-                    __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + c4 * 32;
+                    __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + col;
 #pragma unroll
                     for (int e8 = 0; e8 < 4; ++e8) {
                         uint4 v;
-                        v.x = pack_bf16x2(o[e8 * 8 + 0] * inv, o[e8 * 8 + 1] * inv);
-                        v.y = pack_bf16x2(o[e8 * 8 + 2] * inv, o[e8 * 8 + 3] * inv);
-                        v.z = pack_bf16x2(o[e8 * 8 + 4] * inv, o[e8 * 8 + 5] * inv);
-                        v.w = pack_bf16x2(o[e8 * 8 + 6] * inv, o[e8 * 8 + 7] * inv);
+                        v.x = pack_bf16x2(o0[e8 * 8 + 0] * a0 + o1[e8 * 8 + 0] * a1, o0[e8 * 8 + 1] * a0 + o1[e8 * 8 + 1] * a1);
+                        v.y = pack_bf16x2(o0[e8 * 8 + 2] * a0 + o1[e8 * 8 + 2] * a1, o0[e8 * 8 + 3] * a0 + o1[e8 * 8 + 3] * a1);
+                        v.z = pack_bf16x2(o0[e8 * 8 + 4] * a0 + o1[e8 * 8 + 4] * a1, o0[e8 * 8 + 5] * a0 + o1[e8 * 8 + 5] * a1);
+                        v.w = pack_bf16x2(o0[e8 * 8 + 6] * a0 + o1[e8 * 8 + 6] * a1, o0[e8 * 8 + 7] * a0 + o1[e8 * 8 + 7] * a1);
                         *reinterpret_cast<uint4*>(dst + e8 * 8) = v;
                     }
                 }
@@ -380,7 +410,7 @@ cudaError_t launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     cudaError_t err = allow_dynamic_smem((const void*)kern, smem);
     if (err != cudaSuccess) return err;
     dim3 grid(p.nqblk, p.H_kv, p.B);
-    kern<<<grid, 192, smem, stream>>>(tq, tk, tv, p);
+    kern<<<grid, 320, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
