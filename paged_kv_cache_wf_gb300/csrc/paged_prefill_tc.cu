@@ -32,7 +32,6 @@ namespace {
 
 constexpr int PM = 128;          // rows per CTA
 constexpr int PN = 128;          // keys per tile
-constexpr int kPfStages = 2;
 constexpr float kLazy = 8.f;     // rescale O only when the row max grows by more than 2^8
 
 struct PfParams {
@@ -49,20 +48,20 @@ template <int D, int G>
 struct PfLayout {
     static constexpr int BMQ = PM / G;              // query tokens per CTA
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
+    static constexpr int STAGES = D == 128 ? 3 : 5; // K/V ring depth
     static constexpr int QBYTES = PM * D * 2;
     static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile
     static constexpr int STAGE = 2 * NC * KVHALF;   // K then V
-    static constexpr int PHALF = PM * 128;          // one 64-key column block of P
-    static constexpr int PBYTES = PM * PN * 2;
     static constexpr int q = 0;
     static constexpr int kv = QBYTES;
-    static constexpr int pbuf = kv + kPfStages * STAGE;
-    static constexpr int bars = pbuf + 2 * PBYTES;
-    // q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[half][2], pv_done[half][2]
-    static constexpr int nbars = 1 + 4 * 2 + 2 * 4;
+    static constexpr int bars = kv + STAGES * STAGE;
+    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[half][2], pv_done[half][2]
+    static constexpr int nbars = 1 + 2 * STAGES + 2 * 2 + 2 * 4;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
-    static constexpr int TMEM_COLS = 512;           // S0 [0,128) S1 [128,256) O_0, O_1 from 256
+    // TMEM: S0 [0,128) S1 [128,256) -- P(j) overwrites the S columns it came from --
+    //       then O_0, O_1 from column 256.
+    static constexpr int TMEM_COLS = 512;
     static_assert(total + 1024 <= 232448, "prefill tile exceeds shared memory");
 };
 
@@ -98,8 +97,8 @@ __global__ void __launch_bounds__(320, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
-    uint64_t* kv_empty = kv_full + 2;
-    uint64_t* s_full = kv_empty + 2;
+    uint64_t* kv_empty = kv_full + L::STAGES;
+    uint64_t* s_full = kv_empty + L::STAGES;
     uint64_t* s_free = s_full + 2;
     uint64_t* p_full = s_free + 2;    // [half][parity]
     uint64_t* pv_done = p_full + 4;   // [half][parity]
@@ -113,11 +112,13 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < L::STAGES; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 8);
+            mbar_init(&s_free[i], 1);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&p_full[i], 4);
@@ -139,8 +140,8 @@ __global__ void __launch_bounds__(320, 1)
                 tma_load_3d_nohint(smem + L::q + cb * (PM * 128), &tm_q, cb * 64, h * G, q_begin + i0, q_full);
         }
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            if (j >= 2 && !mbar_wait(&kv_empty[st], ((j >> 1) - 1) & 1)) {
+            const int st = j % L::STAGES;
+            if (j >= L::STAGES && !mbar_wait(&kv_empty[st], ((j / L::STAGES) - 1) & 1)) {
                 if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
                 break;
             }
@@ -185,34 +186,37 @@ __global__ void __launch_bounds__(320, 1)
                     const int u = tp[hh];
                     if (u < tq && mbar_test(&p_full[hh * 2 + (u & 1)], (u >> 1) & 1)) {
                         tc::fence_after_sync();
-                        const uint32_t pbase = smem_u32(smem + L::pbuf + (u & 1) * L::PBYTES + hh * L::PHALF);
-                        const uint32_t vbase = smem_u32(v_tile(u & 1, 0));
+                        // A = P(u) keys [64h, 64h+64) in TMEM (bf16 pairs over the S columns)
+                        const uint32_t pcol = tmem + (u & 1) * 128 + hh * 64;
+                        const uint32_t vbase = smem_u32(v_tile(u % L::STAGES, 0));
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = tc::sdesc_sw128(pbase + kk * 32, 16, 1024);
                             const uint64_t bd = tc::sdesc_sw128(vbase + (4 * hh + kk) * 2048, L::KVHALF, 1024);
-                            tc::mma_f16(tmem + 256 + hh * D, ad, bd, idO, (u > 0 || kk > 0) ? 1u : 0u);
+                            tc::mma_f16_tmem_a(tmem + 256 + hh * D, pcol + kk * 8, bd, idO, (u > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::commit(&pv_done[hh * 2 + (u & 1)]);
-                        if (tp[hh ^ 1] > u) tc::commit(&kv_empty[u & 1]);  // both halves read V(u)
+                        if (tp[hh ^ 1] > u) {  // both halves have consumed V(u) and P(u)
+                            tc::commit(&kv_empty[u % L::STAGES]);
+                            tc::commit(&s_free[u & 1]);
+                        }
                         tp[hh] = u + 1;
                         did = true;
                     }
                 }
                 if (tq < ntiles) {
-                    const int st = tq & 1;
-                    if (mbar_test(&kv_full[st], (tq >> 1) & 1) &&
-                        (tq < 2 || mbar_test(&s_free[st], ((tq >> 1) - 1) & 1))) {
+                    const int st = tq % L::STAGES, sbq = tq & 1;
+                    if (mbar_test(&kv_full[st], (tq / L::STAGES) & 1) &&
+                        (tq < 2 || mbar_test(&s_free[sbq], ((tq >> 1) - 1) & 1))) {
                         tc::fence_after_sync();
                         const uint32_t kbase = smem_u32(k_tile(st, 0));
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
                             const uint32_t koff = (kk >> 2) * L::KVHALF + (kk & 3) * 32;
-                            tc::mma_f16(tmem + st * 128, tc::sdesc_sw128(qbase + off, 16, 1024),
+                            tc::mma_f16(tmem + sbq * 128, tc::sdesc_sw128(qbase + off, 16, 1024),
                                         tc::sdesc_sw128(kbase + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                         }
-                        tc::commit(&s_full[st]);
+                        tc::commit(&s_full[sbq]);
                         ++tq;
                         did = true;
                     }
@@ -255,9 +259,6 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) tc::ld_32cols(tmem + lane_addr + sb * 128 + hh * 64 + c2 * 32, s[c2]);
             tc::wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[sb]);
 
             // keys some row of the CTA may not see: mask them.  The row max is taken
             // on raw scores (scale > 0) and scaled once.
@@ -305,38 +306,31 @@ __global__ void __launch_bounds__(320, 1)
                 tc::wait_st();
             }
             l_run *= alpha;
-            // this half of P buffer sb was last read by P.V of tile j-2
-            if (j >= 2 && !mbar_wait(&pv_done[hh * 2 + sb], ((j - 2) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
-            unsigned char* pt = smem + L::pbuf + sb * L::PBYTES + hh * L::PHALF;
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-m_use, -m_use);
             float2 psum2 = make_float2(0.f, 0.f);
+            uint32_t pw[32];  // keys 64h + 2k, 64h + 2k + 1 as a bf16 pair
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                for (int e8 = 0; e8 < 4; ++e8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
-                        const float2 x = __ffma2_rn(make_float2(s[c2][e8 * 8 + 2 * u], s[c2][e8 * 8 + 2 * u + 1]),
-                                                    sc2, nm2);
-                        const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
-                        psum2 = __fadd2_rn(psum2, e2);
-                        w[u] = pack_bf16x2(e2.x, e2.y);
-                    }
-                    const int chunk = c2 * 4 + e8;  // 8-key chunk within this half
-                    const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(pt + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int u = 0; u < 16; ++u) {
+                    // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
+                    const float2 x = __ffma2_rn(make_float2(s[c2][2 * u], s[c2][2 * u + 1]), sc2, nm2);
+                    const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
+                    psum2 = __fadd2_rn(psum2, e2);
+                    pw[c2 * 16 + u] = pack_bf16x2(e2.x, e2.y);
                 }
             l_run += psum2.x + psum2.y;
+            // P(j) replaces the S columns this half has just read
+            tc::st_32words(tmem + lane_addr + sb * 128 + hh * 64, pw);
+            tc::wait_st();
             // keys past the CTA's end were not loaded (or are stale): zero their V rows.
             // Thread r of half h owns key 64h + (r % 64) and column block r / 64.
             {
                 const int key = hh * 64 + (r & 63), cb = r >> 6;
                 if (cb < L::NC && j * PN + key >= kend) {
-                    uint4* row = reinterpret_cast<uint4*>(v_tile(sb, cb) + (key >> 3) * 1024 + (key & 7) * 128);
+                    uint4* row = reinterpret_cast<uint4*>(v_tile(j % L::STAGES, cb) + (key >> 3) * 1024 + (key & 7) * 128);
 #pragma unroll
                     for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
                 }
