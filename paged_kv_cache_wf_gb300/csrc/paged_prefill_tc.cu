@@ -30,8 +30,8 @@ namespace wf {
 
 namespace {
 
-constexpr int PM = 128;          // rows per CTA
-constexpr int PN = 128;          // keys per tile
+constexpr int PM = 128;          // rows per CTA (TMEM lanes, MMA M)
+constexpr int PN = 64;           // keys per tile
 constexpr float kLazy = 8.f;     // rescale O only when the row max grows by more than 2^8
 
 struct PfParams {
@@ -44,34 +44,37 @@ struct PfParams {
     float scale_log2;
 };
 
+// Two CTAs share an SM: while one runs its softmax the other keeps the tensor
+// cores busy, and one CTA's start-up and drain hide behind the other's work.
 template <int D, int G>
 struct PfLayout {
     static constexpr int BMQ = PM / G;              // query tokens per CTA
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
-    static constexpr int STAGES = D == 128 ? 3 : 5; // K/V ring depth
+    static constexpr int STAGES = D == 128 ? 2 : 4; // K/V ring depth
     static constexpr int QBYTES = PM * D * 2;
-    static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile
+    static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile (8 KB)
     static constexpr int STAGE = 2 * NC * KVHALF;   // K then V
     static constexpr int q = 0;
     static constexpr int kv = QBYTES;
     static constexpr int bars = kv + STAGES * STAGE;
-    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[half][2], pv_done[half][2]
-    static constexpr int nbars = 1 + 2 * STAGES + 2 * 2 + 2 * 4;
+    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[2], pv_done[2]
+    static constexpr int nbars = 1 + 2 * STAGES + 4 * 2;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
-    // TMEM: S0 [0,128) S1 [128,256) -- P(j) overwrites the S columns it came from --
-    //       then O_0, O_1 from column 256.
-    static constexpr int TMEM_COLS = 512;
-    static_assert(total + 1024 <= 232448, "prefill tile exceeds shared memory");
+    // TMEM: S0 [0,64) S1 [64,128) -- P(j) overwrites the first half of its S buffer --
+    //       O [128, 128 + D).
+    static constexpr int TMEM_COLS = 256;
+    static_assert(2 * (total + 1024) <= 233472, "two prefill CTAs must fit on one SM");
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(192, 2)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
     using L = PfLayout<D, G>;
-    const int qb = p.nqblk - 1 - (int)blockIdx.x;   // the longest query blocks start first
-    const int h = blockIdx.y, b = blockIdx.z;
+    const int qb = p.nqblk - 1 - (int)blockIdx.y;   // the longest query blocks start first
+    const int hb = blockIdx.x;                      // (request, KV head)
+    const int h = hb % p.H_kv, b = hb / p.H_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int q_begin = __ldg(p.cu_q_lens + b);
@@ -81,7 +84,7 @@ __global__ void __launch_bounds__(320, 1)
     const bool bad = q_begin < 0 || n < 0 || q_end > p.total_q || n > p.max_q_len || len < n ||
                      len > p.max_seq_len || (int64_t)len > (int64_t)p.M * p.P;
     if (bad) {
-        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
+        if (blockIdx.y == 0 && h == 0 && threadIdx.x == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
         return;
     }
     const int i0 = qb * L::BMQ;
@@ -100,8 +103,8 @@ __global__ void __launch_bounds__(320, 1)
     uint64_t* kv_empty = kv_full + L::STAGES;
     uint64_t* s_full = kv_empty + L::STAGES;
     uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;    // [half][parity]
-    uint64_t* pv_done = p_full + 4;   // [half][parity]
+    uint64_t* p_full = s_free + 2;
+    uint64_t* pv_done = p_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     auto k_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + cb * L::KVHALF; };
     auto v_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + (L::NC + cb) * L::KVHALF; };
@@ -119,8 +122,6 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 1);
-        }
-        for (int i = 0; i < 4; ++i) {
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
         }
@@ -147,12 +148,12 @@ __global__ void __launch_bounds__(320, 1)
             }
             const int k0 = j * PN;
             const int kt = min(PN, kend - k0);
-            const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile
+            const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 4)
             // one 2 KB box per lane: lane = (K or V, column block, 16-key block)
-            const int bx = lane & 7, cb = (lane >> 3) & 1, isv = lane >> 4;
+            const int bx = lane & 3, cb = (lane >> 2) & 1, isv = (lane >> 3) & 1;
             bool okb = false;
             int blk = 0;
-            if (bx < nbox && cb < L::NC) {
+            if (lane < 16 && bx < nbox && cb < L::NC) {
                 const int pos = k0 + bx * 16;
                 blk = __ldg(p.block_tables + (int64_t)b * p.M + pos / p.P);
                 okb = (unsigned)blk < (unsigned)p.N;
@@ -169,54 +170,46 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == 1) {
         // ============================= MMA issuer ===================================
-        // Keys 0-63 and 64-127 of every tile have independent softmax states and
-        // accumulators (half h: O_h += P[:, 64h:64h+64] V[64h:64h+64, :]).
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(PM, D, 0, 1);
             bool ok = mbar_wait(q_full, 0);
             if (!ok) report(p.dev_status, WF_DEV_TIMEOUT);
             const uint32_t qbase = smem_u32(smem + L::q);
-            int tq = 0, tp[2] = {0, 0};
+            int tq = 0, tp = 0;
             uint32_t idle = 0;
-            while (ok && (tp[0] < ntiles || tp[1] < ntiles)) {
+            while (ok && tp < ntiles) {
                 bool did = false;
+                if (tp < tq && mbar_test(&p_full[tp & 1], (tp >> 1) & 1)) {
+                    // O += P(tp) V(tp): A = P in TMEM (bf16 pairs over S's first 32 columns)
+                    tc::fence_after_sync();
+                    const uint32_t pcol = tmem + (tp & 1) * 64;
+                    const uint32_t vbase = smem_u32(v_tile(tp % L::STAGES, 0));
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int u = tp[hh];
-                    if (u < tq && mbar_test(&p_full[hh * 2 + (u & 1)], (u >> 1) & 1)) {
-                        tc::fence_after_sync();
-                        // A = P(u) keys [64h, 64h+64) in TMEM (bf16 pairs over the S columns)
-                        const uint32_t pcol = tmem + (u & 1) * 128 + hh * 64;
-                        const uint32_t vbase = smem_u32(v_tile(u % L::STAGES, 0));
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t bd = tc::sdesc_sw128(vbase + (4 * hh + kk) * 2048, L::KVHALF, 1024);
-                            tc::mma_f16_tmem_a(tmem + 256 + hh * D, pcol + kk * 8, bd, idO, (u > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc::commit(&pv_done[hh * 2 + (u & 1)]);
-                        if (tp[hh ^ 1] > u) {  // both halves have consumed V(u) and P(u)
-                            tc::commit(&kv_empty[u % L::STAGES]);
-                            tc::commit(&s_free[u & 1]);
-                        }
-                        tp[hh] = u + 1;
-                        did = true;
+                    for (int kk = 0; kk < PN / 16; ++kk) {
+                        const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2048, L::KVHALF, 1024);
+                        tc::mma_f16_tmem_a(tmem + 128, pcol + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
                     }
+                    tc::commit(&pv_done[tp & 1]);
+                    tc::commit(&kv_empty[tp % L::STAGES]);
+                    tc::commit(&s_free[tp & 1]);
+                    ++tp;
+                    did = true;
                 }
                 if (tq < ntiles) {
-                    const int st = tq % L::STAGES, sbq = tq & 1;
+                    const int st = tq % L::STAGES, sb = tq & 1;
                     if (mbar_test(&kv_full[st], (tq / L::STAGES) & 1) &&
-                        (tq < 2 || mbar_test(&s_free[sbq], ((tq >> 1) - 1) & 1))) {
+                        (tq < 2 || mbar_test(&s_free[sb], ((tq >> 1) - 1) & 1))) {
                         tc::fence_after_sync();
                         const uint32_t kbase = smem_u32(k_tile(st, 0));
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
                             const uint32_t koff = (kk >> 2) * L::KVHALF + (kk & 3) * 32;
-                            tc::mma_f16(tmem + sbq * 128, tc::sdesc_sw128(qbase + off, 16, 1024),
+                            tc::mma_f16(tmem + sb * 64, tc::sdesc_sw128(qbase + off, 16, 1024),
                                         tc::sdesc_sw128(kbase + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                         }
-                        tc::commit(&s_full[sbq]);
+                        tc::commit(&s_full[sb]);
                         ++tq;
                         did = true;
                     }
@@ -234,8 +227,6 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else {
         // ============================= softmax ======================================
-        // warps 2-5: keys 0-63 of each tile (half 0); warps 6-9: keys 64-127 (half 1).
-        const int hh = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                  // row / TMEM lane
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
@@ -243,12 +234,11 @@ __global__ void __launch_bounds__(320, 1)
         const int qi = i0 + tok;
         const bool row_valid = qi < n;
         const int last_key = c + qi;                     // row sees keys 0 .. last_key
-        const uint32_t o_col = 256 + hh * D;             // this half's accumulator
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
             const int sb = j & 1;
-            const int k0 = j * PN + hh * 64;             // first key of this half
+            const int k0 = j * PN;
             if (!mbar_wait(&s_full[sb], (j >> 1) & 1)) {
                 report(p.dev_status, WF_DEV_TIMEOUT);
                 ok = false;
@@ -257,12 +247,12 @@ __global__ void __launch_bounds__(320, 1)
             tc::fence_after_sync();
             float s[2][32];
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) tc::ld_32cols(tmem + lane_addr + sb * 128 + hh * 64 + c2 * 32, s[c2]);
+            for (int c2 = 0; c2 < 2; ++c2) tc::ld_32cols(tmem + lane_addr + sb * 64 + c2 * 32, s[c2]);
             tc::wait_ld();
 
             // keys some row of the CTA may not see: mask them.  The row max is taken
             // on raw scores (scale > 0) and scaled once.
-            const bool masked = (k0 + 63 > c + i0) || !row_valid;
+            const bool masked = (k0 + PN - 1 > c + i0) || !row_valid;
             float mraw = -INFINITY;
             if (masked) {
 #pragma unroll
@@ -281,7 +271,6 @@ __global__ void __launch_bounds__(320, 1)
             }
             const float mt = mraw * p.scale_log2;
             // lazy online softmax: move the reference max only when it grows by > 2^8
-            // (while nothing has been visible yet, O_h and l are still zero)
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
                 m_ref = mt;
@@ -290,18 +279,17 @@ __global__ void __launch_bounds__(320, 1)
                 m_ref = mt;
             }
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                // O_h must hold P.V of tile j-1 before it is rescaled
-                if (!mbar_wait(&pv_done[hh * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1))
-                    report(p.dev_status, WF_DEV_TIMEOUT);
+                // O must hold P.V of tile j-1 before it is rescaled
+                if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     float o[32];
-                    tc::ld_32cols(tmem + lane_addr + o_col + c4 * 32, o);
+                    tc::ld_32cols(tmem + lane_addr + 128 + c4 * 32, o);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tc::st_32cols(tmem + lane_addr + o_col + c4 * 32, o);
+                    tc::st_32cols(tmem + lane_addr + 128 + c4 * 32, o);
                 }
                 tc::wait_st();
             }
@@ -310,7 +298,7 @@ __global__ void __launch_bounds__(320, 1)
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-m_use, -m_use);
             float2 psum2 = make_float2(0.f, 0.f);
-            uint32_t pw[32];  // keys 64h + 2k, 64h + 2k + 1 as a bf16 pair
+            uint32_t pw[32];  // keys 2k, 2k+1 of the tile as a bf16 pair
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
@@ -322,14 +310,14 @@ __global__ void __launch_bounds__(320, 1)
                     pw[c2 * 16 + u] = pack_bf16x2(e2.x, e2.y);
                 }
             l_run += psum2.x + psum2.y;
-            // P(j) replaces the S columns this half has just read
-            tc::st_32words(tmem + lane_addr + sb * 128 + hh * 64, pw);
+            // P(j) replaces the first 32 S columns of this buffer
+            tc::st_32words(tmem + lane_addr + sb * 64, pw);
             tc::wait_st();
             // keys past the CTA's end were not loaded (or are stale): zero their V rows.
-            // Thread r of half h owns key 64h + (r % 64) and column block r / 64.
+            // Thread r owns key r % 64 of the tile and column block r / 64.
             {
-                const int key = hh * 64 + (r & 63), cb = r >> 6;
-                if (cb < L::NC && j * PN + key >= kend) {
+                const int key = r & 63, cb = r >> 6;
+                if (cb < L::NC && k0 + key >= kend) {
                     uint4* row = reinterpret_cast<uint4*>(v_tile(j % L::STAGES, cb) + (key >> 3) * 1024 + (key & 7) * 128);
 #pragma unroll
                     for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
@@ -338,46 +326,28 @@ __global__ void __launch_bounds__(320, 1)
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[hh * 2 + sb]);
+            if (lane == 0) mbar_arrive(&p_full[sb]);
         }
-        // ---- epilogue: merge the two halves, O / l -> bf16 ------------------------------
-        // The Q tile is no longer read (every S MMA has completed): it holds the
-        // (m, l) exchange between the halves.
-        const int last = ntiles - 1;
-        if (ok && !mbar_wait(&pv_done[hh * 2 + (last & 1)], (last >> 1) & 1)) {
-            report(p.dev_status, WF_DEV_TIMEOUT);
-            ok = false;
-        }
-        float2* xch = reinterpret_cast<float2*>(smem + L::q);
-        xch[hh * PM + r] = make_float2(m_ref, l_run);
-        named_bar_sync(1, 256);
+        // ---- epilogue: O / l -> bf16 --------------------------------------------------
         if (ok) {
-            const float2 other = xch[(hh ^ 1) * PM + r];
-            const float m0 = hh == 0 ? m_ref : other.x, l0 = hh == 0 ? l_run : other.y;
-            const float m1 = hh == 0 ? other.x : m_ref, l1 = hh == 0 ? other.y : l_run;
-            const float m = fmaxf(m0, m1);
-            const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - m);
-            const float w1 = m1 == -INFINITY ? 0.f : ex2(m1 - m);
-            const float inv = row_valid ? 1.f / (l0 * w0 + l1 * w1) : 0.f;
-            const float a0 = w0 * inv, a1 = w1 * inv;
-            // half h stores columns [h*D/2, (h+1)*D/2)
+            const int last = ntiles - 1;
+            if (!mbar_wait(&pv_done[last & 1], (last >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             tc::fence_after_sync();
+            const float inv = row_valid ? 1.f / l_run : 0.f;
 #pragma unroll
-            for (int c4 = 0; c4 < D / 64; ++c4) {
-                const int col = hh * (D / 2) + c4 * 32;
-                float o0[32], o1[32];
-                tc::ld_32cols(tmem + lane_addr + 256 + col, o0);
-                tc::ld_32cols(tmem + lane_addr + 256 + D + col, o1);
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                float o[32];
+                tc::ld_32cols(tmem + lane_addr + 128 + c4 * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
-                    __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + col;
+                    __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + c4 * 32;
 #pragma unroll
                     for (int e8 = 0; e8 < 4; ++e8) {
                         uint4 v;
-                        v.x = pack_bf16x2(o0[e8 * 8 + 0] * a0 + o1[e8 * 8 + 0] * a1, o0[e8 * 8 + 1] * a0 + o1[e8 * 8 + 1] * a1);
-                        v.y = pack_bf16x2(o0[e8 * 8 + 2] * a0 + o1[e8 * 8 + 2] * a1, o0[e8 * 8 + 3] * a0 + o1[e8 * 8 + 3] * a1);
-                        v.z = pack_bf16x2(o0[e8 * 8 + 4] * a0 + o1[e8 * 8 + 4] * a1, o0[e8 * 8 + 5] * a0 + o1[e8 * 8 + 5] * a1);
-                        v.w = pack_bf16x2(o0[e8 * 8 + 6] * a0 + o1[e8 * 8 + 6] * a1, o0[e8 * 8 + 7] * a0 + o1[e8 * 8 + 7] * a1);
+                        v.x = pack_bf16x2(o[e8 * 8 + 0] * inv, o[e8 * 8 + 1] * inv);
+                        v.y = pack_bf16x2(o[e8 * 8 + 2] * inv, o[e8 * 8 + 3] * inv);
+                        v.z = pack_bf16x2(o[e8 * 8 + 4] * inv, o[e8 * 8 + 5] * inv);
+                        v.w = pack_bf16x2(o[e8 * 8 + 6] * inv, o[e8 * 8 + 7] * inv);
                         *reinterpret_cast<uint4*>(dst + e8 * 8) = v;
                     }
                 }
@@ -403,8 +373,8 @@ cudaError_t launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     auto kern = paged_prefill_tc_kernel<D, G>;
     cudaError_t err = allow_dynamic_smem((const void*)kern, smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(p.nqblk, p.H_kv, p.B);
-    kern<<<grid, 320, smem, stream>>>(tq, tk, tv, p);
+    dim3 grid(p.B * p.H_kv, p.nqblk);
+    kern<<<grid, 192, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
