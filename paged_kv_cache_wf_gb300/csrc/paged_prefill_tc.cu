@@ -53,6 +53,12 @@ struct PfLayout {
     static constexpr int STAGES = D == 128 ? 2 : 4; // K/V ring depth
     static constexpr int QBYTES = PM * D * 2;
     static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile (8 KB)
+    // D = 128: one 4 KB box per 16-key block holds both 64-wide halves, laid out
+    // [8-key group][half][8 keys][64 d] -- atoms 2048 B apart, halves 1024 B apart.
+    // D = 64: one 2 KB box per block, [16 keys][64 d] -- atoms 1024 B apart.
+    static constexpr int ATOM = NC == 2 ? 2048 : 1024;   // stride between 8-key atoms
+    static constexpr int HALF_OFF = 1024;                 // offset of the second 64-wide half
+    static constexpr int BOX = NC * 2048;                 // bytes of one block's box
     static constexpr int STAGE = 2 * NC * KVHALF;   // K then V
     static constexpr int q = 0;
     static constexpr int kv = QBYTES;
@@ -106,8 +112,8 @@ __global__ void __launch_bounds__(192, 2)
     uint64_t* p_full = s_free + 2;
     uint64_t* pv_done = p_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
-    auto k_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + cb * L::KVHALF; };
-    auto v_tile = [&](int st, int cb) { return smem + L::kv + st * L::STAGE + (L::NC + cb) * L::KVHALF; };
+    auto k_tile = [&](int st) { return smem + L::kv + st * L::STAGE; };
+    auto v_tile = [&](int st) { return smem + L::kv + st * L::STAGE + L::NC * L::KVHALF; };
 
     if (warp == 1) {
         tc::alloc(tmem_slot, L::TMEM_COLS);
@@ -149,23 +155,27 @@ __global__ void __launch_bounds__(192, 2)
             const int k0 = j * PN;
             const int kt = min(PN, kend - k0);
             const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 4)
-            // one 2 KB box per lane: lane = (K or V, column block, 16-key block)
-            const int bx = lane & 3, cb = (lane >> 2) & 1, isv = (lane >> 3) & 1;
+            // one box per lane: lanes 0-3 K of block 0-3, lanes 4-7 V of block 0-3
+            const int bx = lane & 3, isv = (lane >> 2) & 1;
             bool okb = false;
             int blk = 0;
-            if (lane < 16 && bx < nbox && cb < L::NC) {
+            if (lane < 8 && bx < nbox) {
                 const int pos = k0 + bx * 16;
                 blk = __ldg(p.block_tables + (int64_t)b * p.M + pos / p.P);
                 okb = (unsigned)blk < (unsigned)p.N;
-                if (!okb && cb == 0 && isv == 0) report(p.dev_status, WF_DEV_BAD_BLOCK);
+                if (!okb && isv == 0) report(p.dev_status, WF_DEV_BAD_BLOCK);
             }
             const unsigned okm = __ballot_sync(0xffffffffu, okb);
-            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)__popc(okm) * 2048u);
+            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)__popc(okm) * (uint32_t)L::BOX);
             __syncwarp();
             if (okb) {
-                const int slot = blk * p.P + (k0 + bx * 16) % p.P;
-                unsigned char* dst = (isv ? v_tile(st, cb) : k_tile(st, cb)) + bx * 2048;
-                tma_load_3d_nohint(dst, isv ? &tm_v : &tm_k, cb * 64, slot, h, &kv_full[st]);
+                const int slot = blk * p.P + (k0 + bx * 16) % p.P;   // multiple of 16
+                unsigned char* dst = (isv ? v_tile(st) : k_tile(st)) + bx * L::BOX;
+                if constexpr (L::NC == 2) {
+                    tma_load_5d(dst, isv ? &tm_v : &tm_k, 0, 0, 0, slot >> 3, h, &kv_full[st]);
+                } else {
+                    tma_load_3d_nohint(dst, isv ? &tm_v : &tm_k, 0, slot, h, &kv_full[st]);
+                }
             }
         }
     } else if (warp == 1) {
@@ -184,10 +194,11 @@ __global__ void __launch_bounds__(192, 2)
                     // O += P(tp) V(tp): A = P in TMEM (bf16 pairs over S's first 32 columns)
                     tc::fence_after_sync();
                     const uint32_t pcol = tmem + (tp & 1) * 64;
-                    const uint32_t vbase = smem_u32(v_tile(tp % L::STAGES, 0));
+                    const uint32_t vbase = smem_u32(v_tile(tp % L::STAGES));
 #pragma unroll
                     for (int kk = 0; kk < PN / 16; ++kk) {
-                        const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2048, L::KVHALF, 1024);
+                        // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
+                        const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2 * L::ATOM, L::HALF_OFF, L::ATOM);
                         tc::mma_f16_tmem_a(tmem + 128, pcol + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::commit(&pv_done[tp & 1]);
@@ -201,13 +212,13 @@ __global__ void __launch_bounds__(192, 2)
                     if (mbar_test(&kv_full[st], (tq / L::STAGES) & 1) &&
                         (tq < 2 || mbar_test(&s_free[sb], ((tq >> 1) - 1) & 1))) {
                         tc::fence_after_sync();
-                        const uint32_t kbase = smem_u32(k_tile(st, 0));
+                        const uint32_t kbase = smem_u32(k_tile(st));
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
-                            const uint32_t koff = (kk >> 2) * L::KVHALF + (kk & 3) * 32;
+                            const uint32_t koff = (kk >> 2) * L::HALF_OFF + (kk & 3) * 32;
                             tc::mma_f16(tmem + sb * 64, tc::sdesc_sw128(qbase + off, 16, 1024),
-                                        tc::sdesc_sw128(kbase + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                                        tc::sdesc_sw128(kbase + koff, 16, L::ATOM), idS, kk > 0 ? 1u : 0u);
                         }
                         tc::commit(&s_full[sb]);
                         ++tq;
@@ -318,7 +329,8 @@ __global__ void __launch_bounds__(192, 2)
             {
                 const int key = r & 63, cb = r >> 6;
                 if (cb < L::NC && k0 + key >= kend) {
-                    uint4* row = reinterpret_cast<uint4*>(v_tile(j % L::STAGES, cb) + (key >> 3) * 1024 + (key & 7) * 128);
+                    uint4* row = reinterpret_cast<uint4*>(v_tile(j % L::STAGES) + (key >> 3) * L::ATOM +
+                                                          cb * L::HALF_OFF + (key & 7) * 128);
 #pragma unroll
                     for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -406,12 +418,25 @@ cudaError_t launch_paged_prefill_tc(void* out, const void* q, const void* k_pool
     }
     {
         const uint64_t slots = (uint64_t)pool.num_blocks * pool.block_size;
-        const uint64_t dims[3] = {(uint64_t)D, slots, (uint64_t)pool.num_kv_heads};
-        const uint64_t strides[2] = {(uint64_t)pool.num_kv_heads * D * 2, (uint64_t)D * 2};
-        const uint32_t box[3] = {64, 16, 1};
-        cudaError_t e = encode_tiled_bf16(&tk, const_cast<void*>(k_pool), 3, dims, strides, box);
-        if (e != cudaSuccess) return e;
-        e = encode_tiled_bf16(&tv, const_cast<void*>(v_pool), 3, dims, strides, box);
+        const uint64_t row = (uint64_t)pool.num_kv_heads * D * 2;   // bytes of one pool slot
+        cudaError_t e;
+        if (D == 128) {
+            // (d 0-63, slot % 8, d half, slot / 8, head): a 16-slot box of one head holds both
+            // halves of D as [slot/8 % 2][half][slot % 8][64]
+            const uint64_t dims[5] = {64, 8, 2, slots / 8, (uint64_t)pool.num_kv_heads};
+            const uint64_t strides[4] = {row, 128, 8 * row, (uint64_t)D * 2};
+            const uint32_t box[5] = {64, 8, 2, 2, 1};
+            e = encode_tiled_bf16(&tk, const_cast<void*>(k_pool), 5, dims, strides, box);
+            if (e != cudaSuccess) return e;
+            e = encode_tiled_bf16(&tv, const_cast<void*>(v_pool), 5, dims, strides, box);
+        } else {
+            const uint64_t dims[3] = {(uint64_t)D, slots, (uint64_t)pool.num_kv_heads};
+            const uint64_t strides[2] = {row, (uint64_t)D * 2};
+            const uint32_t box[3] = {64, 16, 1};
+            e = encode_tiled_bf16(&tk, const_cast<void*>(k_pool), 3, dims, strides, box);
+            if (e != cudaSuccess) return e;
+            e = encode_tiled_bf16(&tv, const_cast<void*>(v_pool), 3, dims, strides, box);
+        }
         if (e != cudaSuccess) return e;
     }
     PfParams p;
