@@ -44,13 +44,13 @@ struct PfParams {
     float scale_log2;
 };
 
-// Two CTAs share an SM: while one runs its softmax the other keeps the tensor
-// cores busy, and one CTA's start-up and drain hide behind the other's work.
+// One CTA per SM with a deep K/V ring: a TMA round trip (~1 us) is longer than
+// the softmax of a 64-key tile (~0.6 us), so loads run several tiles ahead.
 template <int D, int G>
 struct PfLayout {
     static constexpr int BMQ = PM / G;              // query tokens per CTA
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
-    static constexpr int STAGES = D == 128 ? 2 : 4; // K/V ring depth
+    static constexpr int STAGES = D == 128 ? 6 : 8; // K/V ring depth
     static constexpr int QBYTES = PM * D * 2;
     static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile (8 KB)
     // D = 128: one 4 KB box per 16-key block holds both 64-wide halves, laid out
@@ -63,18 +63,20 @@ struct PfLayout {
     static constexpr int q = 0;
     static constexpr int kv = QBYTES;
     static constexpr int bars = kv + STAGES * STAGE;
-    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[2], pv_done[2]
-    static constexpr int nbars = 1 + 2 * STAGES + 4 * 2;
+    static constexpr int NS = 4;                    // S/P buffers in TMEM
+    // q_full, kv_full[S], kv_empty[S], s_full[NS], s_free[NS], p_full[NS], pv_done[NS]
+    static constexpr int nbars = 1 + 2 * STAGES + 4 * NS;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
-    // TMEM: S0 [0,64) S1 [64,128) -- P(j) overwrites the first half of its S buffer --
-    //       O [128, 128 + D).
-    static constexpr int TMEM_COLS = 256;
-    static_assert(2 * (total + 1024) <= 233472, "two prefill CTAs must fit on one SM");
+    // TMEM: S buffers [64 i, 64 i + 64), i < NS -- P(j) overwrites the first half of its
+    //       S buffer -- then O [256, 256 + D).
+    static constexpr int OCOL = NS * 64;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(total + 1024 <= 232448, "prefill CTA exceeds shared memory");
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(192, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
     using L = PfLayout<D, G>;
@@ -108,9 +110,9 @@ __global__ void __launch_bounds__(192, 2)
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + L::STAGES;
     uint64_t* s_full = kv_empty + L::STAGES;
-    uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;
-    uint64_t* pv_done = p_full + 2;
+    uint64_t* s_free = s_full + L::NS;
+    uint64_t* p_full = s_free + L::NS;
+    uint64_t* pv_done = p_full + L::NS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     auto k_tile = [&](int st) { return smem + L::kv + st * L::STAGE; };
     auto v_tile = [&](int st) { return smem + L::kv + st * L::STAGE + L::NC * L::KVHALF; };
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(192, 2)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < L::NS; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 1);
             mbar_init(&p_full[i], 4);
@@ -190,27 +192,27 @@ __global__ void __launch_bounds__(192, 2)
             uint32_t idle = 0;
             while (ok && tp < ntiles) {
                 bool did = false;
-                if (tp < tq && mbar_test(&p_full[tp & 1], (tp >> 1) & 1)) {
+                if (tp < tq && mbar_test(&p_full[tp % L::NS], (tp / L::NS) & 1)) {
                     // O += P(tp) V(tp): A = P in TMEM (bf16 pairs over S's first 32 columns)
                     tc::fence_after_sync();
-                    const uint32_t pcol = tmem + (tp & 1) * 64;
+                    const uint32_t pcol = tmem + (tp % L::NS) * 64;
                     const uint32_t vbase = smem_u32(v_tile(tp % L::STAGES));
 #pragma unroll
                     for (int kk = 0; kk < PN / 16; ++kk) {
                         // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
                         const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2 * L::ATOM, L::HALF_OFF, L::ATOM);
-                        tc::mma_f16_tmem_a(tmem + 128, pcol + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_f16_tmem_a(tmem + L::OCOL, pcol + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc::commit(&pv_done[tp & 1]);
+                    tc::commit(&pv_done[tp % L::NS]);
                     tc::commit(&kv_empty[tp % L::STAGES]);
-                    tc::commit(&s_free[tp & 1]);
+                    tc::commit(&s_free[tp % L::NS]);
                     ++tp;
                     did = true;
                 }
                 if (tq < ntiles) {
-                    const int st = tq % L::STAGES, sb = tq & 1;
+                    const int st = tq % L::STAGES, sb = tq % L::NS;
                     if (mbar_test(&kv_full[st], (tq / L::STAGES) & 1) &&
-                        (tq < 2 || mbar_test(&s_free[sb], ((tq >> 1) - 1) & 1))) {
+                        (tq < L::NS || mbar_test(&s_free[sb], ((tq / L::NS) - 1) & 1))) {
                         tc::fence_after_sync();
                         const uint32_t kbase = smem_u32(k_tile(st));
 #pragma unroll
@@ -248,9 +250,9 @@ __global__ void __launch_bounds__(192, 2)
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
-            const int sb = j & 1;
+            const int sb = j % L::NS;
             const int k0 = j * PN;
-            if (!mbar_wait(&s_full[sb], (j >> 1) & 1)) {
+            if (!mbar_wait(&s_full[sb], (j / L::NS) & 1)) {
                 report(p.dev_status, WF_DEV_TIMEOUT);
                 ok = false;
                 break;
@@ -264,7 +266,6 @@ __global__ void __launch_bounds__(192, 2)
             // keys some row of the CTA may not see: mask them.  The row max is taken
             // on raw scores (scale > 0) and scaled once.
             const bool masked = (k0 + PN - 1 > c + i0) || !row_valid;
-            float mraw = -INFINITY;
             if (masked) {
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2)
@@ -272,14 +273,18 @@ __global__ void __launch_bounds__(192, 2)
                     for (int e = 0; e < 32; ++e) {
                         const bool vis = row_valid && k0 + c2 * 32 + e <= last_key;
                         s[c2][e] = vis ? s[c2][e] : -INFINITY;
-                        mraw = fmaxf(mraw, s[c2][e]);
                     }
-            } else {
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) mraw = fmaxf(mraw, s[c2][e]);
             }
+            // tree of 8 independent running maxima (short dependency chains)
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = fmaxf(s[0][e], s[1][e]);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+                for (int e = 8; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[c2][e]);
+            const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float mt = mraw * p.scale_log2;
             // lazy online softmax: move the reference max only when it grows by > 2^8
             float alpha = 1.f;
@@ -291,16 +296,16 @@ __global__ void __launch_bounds__(192, 2)
             }
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
                 // O must hold P.V of tile j-1 before it is rescaled
-                if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (!mbar_wait(&pv_done[(j - 1) % L::NS], ((j - 1) / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     float o[32];
-                    tc::ld_32cols(tmem + lane_addr + 128 + c4 * 32, o);
+                    tc::ld_32cols(tmem + lane_addr + L::OCOL + c4 * 32, o);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tc::st_32cols(tmem + lane_addr + 128 + c4 * 32, o);
+                    tc::st_32cols(tmem + lane_addr + L::OCOL + c4 * 32, o);
                 }
                 tc::wait_st();
             }
@@ -308,7 +313,8 @@ __global__ void __launch_bounds__(192, 2)
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             const float2 nm2 = make_float2(-m_use, -m_use);
-            float2 psum2 = make_float2(0.f, 0.f);
+            float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
             uint32_t pw[32];  // keys 2k, 2k+1 of the tile as a bf16 pair
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2)
@@ -317,10 +323,12 @@ __global__ void __launch_bounds__(192, 2)
                     // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
                     const float2 x = __ffma2_rn(make_float2(s[c2][2 * u], s[c2][2 * u + 1]), sc2, nm2);
                     const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
-                    psum2 = __fadd2_rn(psum2, e2);
+                    ps[u & 3] = __fadd2_rn(ps[u & 3], e2);
                     pw[c2 * 16 + u] = pack_bf16x2(e2.x, e2.y);
                 }
-            l_run += psum2.x + psum2.y;
+            const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
+            const float2 pst = __fadd2_rn(ps01, ps23);
+            l_run += pst.x + pst.y;
             // P(j) replaces the first 32 S columns of this buffer
             tc::st_32words(tmem + lane_addr + sb * 64, pw);
             tc::wait_st();
@@ -343,13 +351,13 @@ __global__ void __launch_bounds__(192, 2)
         // ---- epilogue: O / l -> bf16 --------------------------------------------------
         if (ok) {
             const int last = ntiles - 1;
-            if (!mbar_wait(&pv_done[last & 1], (last >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            if (!mbar_wait(&pv_done[last % L::NS], (last / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             tc::fence_after_sync();
             const float inv = row_valid ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 float o[32];
-                tc::ld_32cols(tmem + lane_addr + 128 + c4 * 32, o);
+                tc::ld_32cols(tmem + lane_addr + L::OCOL + c4 * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
                     __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + c4 * 32;
