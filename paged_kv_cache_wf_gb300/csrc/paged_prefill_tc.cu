@@ -33,6 +33,8 @@ namespace {
 constexpr int PM = 128;          // rows per CTA (TMEM lanes, MMA M)
 constexpr int PN = 64;           // keys per tile
 constexpr float kLazy = 8.f;     // rescale O only when the row max grows by more than 2^8
+constexpr int kProd = 4;         // producer warps: tile j is issued by warp j % kProd
+constexpr int kThreads = (kProd + 1 + 4) * 32;
 
 struct PfParams {
     __nv_bfloat16* out;
@@ -50,7 +52,8 @@ template <int D, int G>
 struct PfLayout {
     static constexpr int BMQ = PM / G;              // query tokens per CTA
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
-    static constexpr int STAGES = D == 128 ? 6 : 8; // K/V ring depth
+    static constexpr int STAGES = D == 128 ? 5 : 8; // K/V ring depth
+    static constexpr int TBL = 2048;                // block-table entries staged in shared memory
     static constexpr int QBYTES = PM * D * 2;
     static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile (8 KB)
     // D = 128: one 4 KB box per 16-key block holds both 64-wide halves, laid out
@@ -62,7 +65,8 @@ struct PfLayout {
     static constexpr int STAGE = 2 * NC * KVHALF;   // K then V
     static constexpr int q = 0;
     static constexpr int kv = QBYTES;
-    static constexpr int bars = kv + STAGES * STAGE;
+    static constexpr int tbl = kv + STAGES * STAGE;
+    static constexpr int bars = tbl + TBL * 4;
     static constexpr int NS = 4;                    // S/P buffers in TMEM
     // q_full, kv_full[S], kv_empty[S], s_full[NS], s_free[NS], p_full[NS], pv_done[NS]
     static constexpr int nbars = 1 + 2 * STAGES + 4 * NS;
@@ -76,7 +80,7 @@ struct PfLayout {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
     using L = PfLayout<D, G>;
@@ -114,10 +118,11 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* p_full = s_free + L::NS;
     uint64_t* pv_done = p_full + L::NS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
+    int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::tbl);
     auto k_tile = [&](int st) { return smem + L::kv + st * L::STAGE; };
     auto v_tile = [&](int st) { return smem + L::kv + st * L::STAGE + L::NC * L::KVHALF; };
 
-    if (warp == 1) {
+    if (warp == kProd) {
         tc::alloc(tmem_slot, L::TMEM_COLS);
         tc::relinquish();
     }
@@ -140,30 +145,40 @@ __global__ void __launch_bounds__(192, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ============================= producer =====================================
-        if (lane == 0) {
+    if (warp < kProd) {
+        // ============================= producers ====================================
+        // A thread's TMA copies complete one after another, so consecutive tiles are
+        // issued by different warps (tile j by warp j % kProd) to keep several in flight.
+        if (warp == 0 && lane == 0) {
             mbar_arrive_expect_tx(q_full, (uint32_t)L::QBYTES);
 #pragma unroll
             for (int cb = 0; cb < L::NC; ++cb)
                 tma_load_3d_nohint(smem + L::q + cb * (PM * 128), &tm_q, cb * 64, h * G, q_begin + i0, q_full);
         }
-        for (int j = 0; j < ntiles; ++j) {
+        // the CTA's block-table slice, staged once when it fits
+        const int nblk = (kend + p.P - 1) / p.P;
+        const int32_t* trow = p.block_tables + (int64_t)b * p.M;
+        const bool staged = nblk <= L::TBL;
+        if (staged) {
+            for (int i = threadIdx.x; i < nblk; i += kProd * 32) tbl[i] = __ldg(trow + i);
+            named_bar_sync(2, kProd * 32);
+        }
+        for (int j = warp; j < ntiles; j += kProd) {
             const int st = j % L::STAGES;
+            const int k0 = j * PN;
+            const int kt = min(PN, kend - k0);
+            const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 4)
             if (j >= L::STAGES && !mbar_wait(&kv_empty[st], ((j / L::STAGES) - 1) & 1)) {
                 if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
                 break;
             }
-            const int k0 = j * PN;
-            const int kt = min(PN, kend - k0);
-            const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 4)
             // one box per lane: lanes 0-3 K of block 0-3, lanes 4-7 V of block 0-3
             const int bx = lane & 3, isv = (lane >> 2) & 1;
             bool okb = false;
             int blk = 0;
             if (lane < 8 && bx < nbox) {
-                const int pos = k0 + bx * 16;
-                blk = __ldg(p.block_tables + (int64_t)b * p.M + pos / p.P);
+                const int bi = (k0 + bx * 16) / p.P;
+                blk = staged ? tbl[bi] : __ldg(trow + bi);
                 okb = (unsigned)blk < (unsigned)p.N;
                 if (!okb && isv == 0) report(p.dev_status, WF_DEV_BAD_BLOCK);
             }
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kProd) {
         // ============================= MMA issuer ===================================
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
@@ -377,7 +392,7 @@ __global__ void __launch_bounds__(192, 1)
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kProd) {
         __syncwarp();
         tc::fence_after_sync();
         tc::dealloc(tmem, L::TMEM_COLS);
@@ -394,7 +409,7 @@ cudaError_t launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     cudaError_t err = allow_dynamic_smem((const void*)kern, smem);
     if (err != cudaSuccess) return err;
     dim3 grid(p.B * p.H_kv, p.nqblk);
-    kern<<<grid, 192, smem, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
