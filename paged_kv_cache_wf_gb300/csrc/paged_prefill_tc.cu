@@ -33,8 +33,12 @@ namespace {
 constexpr int PM = 128;          // rows per CTA (TMEM lanes, MMA M)
 constexpr int PN = 64;           // keys per tile
 constexpr float kLazy = 8.f;     // rescale O only when the row max grows by more than 2^8
-constexpr int kProd = 4;         // producer warps: tile j is issued by warp j % kProd
-constexpr int kThreads = (kProd + 1 + 4) * 32;
+// warps 0-7 softmax (two warpgroups, one per query tile), then kProd producer warps,
+// then the MMA warp.  12 warps leave 168 registers per thread.
+constexpr int kSoft = 8;
+constexpr int kProd = 3;         // producer warps: tile j is issued by producer j % kProd
+constexpr int kMma = kSoft + kProd;
+constexpr int kThreads = (kMma + 1) * 32;
 
 struct PfParams {
     __nv_bfloat16* out;
@@ -46,15 +50,19 @@ struct PfParams {
     float scale_log2;
 };
 
-// One CTA per SM with a deep K/V ring: a TMA round trip (~1 us) is longer than
-// the softmax of a 64-key tile (~0.6 us), so loads run several tiles ahead.
+// One CTA per SM.  Two 128-row query tiles (A, B) share every K/V tile, which
+// doubles the work per loaded byte; each tile has its own softmax warpgroup, its own
+// S/P ring and O accumulator in TMEM, so one group's exponentials overlap the other
+// group's MMAs.  A deep K/V ring covers the ~1 us TMA round trip.
 template <int D, int G>
 struct PfLayout {
-    static constexpr int BMQ = PM / G;              // query tokens per CTA
+    static constexpr int QT = 2;                    // query tiles per CTA
+    static constexpr int TOKT = PM / G;             // query tokens per tile
+    static constexpr int BMQ = QT * TOKT;           // query tokens per CTA
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
-    static constexpr int STAGES = D == 128 ? 5 : 8; // K/V ring depth
+    static constexpr int STAGES = D == 128 ? 4 : 8; // K/V ring depth
     static constexpr int TBL = 2048;                // block-table entries staged in shared memory
-    static constexpr int QBYTES = PM * D * 2;
+    static constexpr int QTILE = PM * D * 2;        // one query tile
     static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile (8 KB)
     // D = 128: one 4 KB box per 16-key block holds both 64-wide halves, laid out
     // [8-key group][half][8 keys][64 d] -- atoms 2048 B apart, halves 1024 B apart.
@@ -64,16 +72,18 @@ struct PfLayout {
     static constexpr int BOX = NC * 2048;                 // bytes of one block's box
     static constexpr int STAGE = 2 * NC * KVHALF;   // K then V
     static constexpr int q = 0;
-    static constexpr int kv = QBYTES;
+    static constexpr int kv = QT * QTILE;
     static constexpr int tbl = kv + STAGES * STAGE;
     static constexpr int bars = tbl + TBL * 4;
-    static constexpr int NS = 4;                    // S/P buffers in TMEM
-    // q_full, kv_full[S], kv_empty[S], s_full[NS], s_free[NS], p_full[NS], pv_done[NS]
-    static constexpr int nbars = 1 + 2 * STAGES + 4 * NS;
+    static constexpr int NS = 2;                    // S/P buffers per query tile
+    // q_full, kv_full[S], kv_empty[S], then per query tile: s_full[NS], s_free[NS],
+    // p_full[NS], pv_done[NS]
+    static constexpr int nbars = 1 + 2 * STAGES + QT * 4 * NS;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
-    // TMEM: S buffers [64 i, 64 i + 64), i < NS -- P(j) overwrites the first half of its
-    //       S buffer -- then O [256, 256 + D).
+    // TMEM per query tile t, base 256 t: S buffers [64 i, 64 i + 64) for i < NS -- P(j)
+    // overwrites the first half of its S buffer -- then O [128, 128 + D).
+    static constexpr int TCOLS = 256;
     static constexpr int OCOL = NS * 64;
     static constexpr int TMEM_COLS = 512;
     static_assert(total + 1024 <= 232448, "prefill CTA exceeds shared memory");
@@ -105,6 +115,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_tok = min(L::BMQ, n - i0);
     const int kend = c + i0 + rows_tok;               // keys this CTA needs: [0, kend)
     const int ntiles = (kend + PN - 1) / PN;
+    // K/V tiles query tile t takes part in: those holding keys its rows see (0 when
+    // the tile has no query rows; tile 0 always has some)
+    int nt_t[L::QT];
+#pragma unroll
+    for (int t = 0; t < L::QT; ++t) {
+        const int toks = min(L::TOKT, rows_tok - t * L::TOKT);
+        nt_t[t] = toks > 0 ? (c + i0 + t * L::TOKT + toks + PN - 1) / PN : 0;
+    }
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -113,16 +131,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + L::STAGES;
-    uint64_t* s_full = kv_empty + L::STAGES;
-    uint64_t* s_free = s_full + L::NS;
-    uint64_t* p_full = s_free + L::NS;
-    uint64_t* pv_done = p_full + L::NS;
+    uint64_t* tb = kv_empty + L::STAGES;              // per query tile: 4 * NS barriers
+    auto s_full = [&](int t, int i) { return tb + t * 4 * L::NS + i; };
+    auto s_free = [&](int t, int i) { return tb + t * 4 * L::NS + L::NS + i; };
+    auto p_full = [&](int t, int i) { return tb + t * 4 * L::NS + 2 * L::NS + i; };
+    auto pv_done = [&](int t, int i) { return tb + t * 4 * L::NS + 3 * L::NS + i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::tbl);
     auto k_tile = [&](int st) { return smem + L::kv + st * L::STAGE; };
     auto v_tile = [&](int st) { return smem + L::kv + st * L::STAGE + L::NC * L::KVHALF; };
 
-    if (warp == kProd) {
+    if (warp == kMma) {
         tc::alloc(tmem_slot, L::TMEM_COLS);
         tc::relinquish();
     }
@@ -132,12 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
-        for (int i = 0; i < L::NS; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 1);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&pv_done[i], 1);
-        }
+        for (int t = 0; t < L::QT; ++t)
+            for (int i = 0; i < L::NS; ++i) {
+                mbar_init(s_full(t, i), 1);
+                mbar_init(s_free(t, i), 1);
+                mbar_init(p_full(t, i), 4);
+                mbar_init(pv_done(t, i), 1);
+            }
         fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -145,25 +165,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < kProd) {
+    if (warp >= kSoft && warp < kMma) {
         // ============================= producers ====================================
         // A thread's TMA copies complete one after another, so consecutive tiles are
-        // issued by different warps (tile j by warp j % kProd) to keep several in flight.
-        if (warp == 0 && lane == 0) {
-            mbar_arrive_expect_tx(q_full, (uint32_t)L::QBYTES);
+        // issued by different warps (tile j by producer j % kProd) to keep several in flight.
+        const int pw = warp - kSoft;                     // producer index
+        if (pw == 0 && lane == 0) {
+            mbar_arrive_expect_tx(q_full, (uint32_t)(L::QT * L::QTILE));
 #pragma unroll
-            for (int cb = 0; cb < L::NC; ++cb)
-                tma_load_3d_nohint(smem + L::q + cb * (PM * 128), &tm_q, cb * 64, h * G, q_begin + i0, q_full);
+            for (int t = 0; t < L::QT; ++t)
+#pragma unroll
+                for (int cb = 0; cb < L::NC; ++cb)
+                    tma_load_3d_nohint(smem + L::q + t * L::QTILE + cb * (PM * 128), &tm_q, cb * 64, h * G,
+                                       q_begin + i0 + t * L::TOKT, q_full);
         }
         // the CTA's block-table slice, staged once when it fits
         const int nblk = (kend + p.P - 1) / p.P;
         const int32_t* trow = p.block_tables + (int64_t)b * p.M;
         const bool staged = nblk <= L::TBL;
         if (staged) {
-            for (int i = threadIdx.x; i < nblk; i += kProd * 32) tbl[i] = __ldg(trow + i);
+            for (int i = threadIdx.x - kSoft * 32; i < nblk; i += kProd * 32) tbl[i] = __ldg(trow + i);
             named_bar_sync(2, kProd * 32);
         }
-        for (int j = warp; j < ntiles; j += kProd) {
+        for (int j = pw; j < ntiles; j += kProd) {
             const int st = j % L::STAGES;
             const int k0 = j * PN;
             const int kt = min(PN, kend - k0);
@@ -195,51 +219,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == kProd) {
+    } else if (warp == kMma) {
         // ============================= MMA issuer ===================================
+        // Event loop over two query tiles: O_t += P_t(j) V_j as soon as the weights are
+        // ready, else S_t(j) = Q_t K_j^T as soon as tile j has landed and an S buffer
+        // of tile t is free.  K/V stage j is released once every tile that uses it is done.
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
             constexpr uint32_t idO = tc::idesc_bf16_f32(PM, D, 0, 1);
             bool ok = mbar_wait(q_full, 0);
             if (!ok) report(p.dev_status, WF_DEV_TIMEOUT);
             const uint32_t qbase = smem_u32(smem + L::q);
-            int tq = 0, tp = 0;
+            int tq[L::QT], tp[L::QT];
+#pragma unroll
+            for (int t = 0; t < L::QT; ++t) tq[t] = tp[t] = 0;
             uint32_t idle = 0;
-            while (ok && tp < ntiles) {
+            while (ok && (tp[0] < nt_t[0] || tp[1] < nt_t[1])) {
                 bool did = false;
-                if (tp < tq && mbar_test(&p_full[tp % L::NS], (tp / L::NS) & 1)) {
-                    // O += P(tp) V(tp): A = P in TMEM (bf16 pairs over S's first 32 columns)
-                    tc::fence_after_sync();
-                    const uint32_t pcol = tmem + (tp % L::NS) * 64;
-                    const uint32_t vbase = smem_u32(v_tile(tp % L::STAGES));
 #pragma unroll
-                    for (int kk = 0; kk < PN / 16; ++kk) {
-                        // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
-                        const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2 * L::ATOM, L::HALF_OFF, L::ATOM);
-                        tc::mma_f16_tmem_a(tmem + L::OCOL, pcol + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::commit(&pv_done[tp % L::NS]);
-                    tc::commit(&kv_empty[tp % L::STAGES]);
-                    tc::commit(&s_free[tp % L::NS]);
-                    ++tp;
-                    did = true;
-                }
-                if (tq < ntiles) {
-                    const int st = tq % L::STAGES, sb = tq % L::NS;
-                    if (mbar_test(&kv_full[st], (tq / L::STAGES) & 1) &&
-                        (tq < L::NS || mbar_test(&s_free[sb], ((tq / L::NS) - 1) & 1))) {
+                for (int t = 0; t < L::QT; ++t) {
+                    const int u = tp[t];
+                    if (u < tq[t] && mbar_test(p_full(t, u % L::NS), (u / L::NS) & 1)) {
                         tc::fence_after_sync();
-                        const uint32_t kbase = smem_u32(k_tile(st));
+                        const uint32_t pcol = tmem + t * L::TCOLS + (u % L::NS) * 64;
+                        const uint32_t vbase = smem_u32(v_tile(u % L::STAGES));
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
-                            const uint32_t koff = (kk >> 2) * L::HALF_OFF + (kk & 3) * 32;
-                            tc::mma_f16(tmem + sb * 64, tc::sdesc_sw128(qbase + off, 16, 1024),
-                                        tc::sdesc_sw128(kbase + koff, 16, L::ATOM), idS, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < PN / 16; ++kk) {
+                            // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
+                            const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2 * L::ATOM, L::HALF_OFF, L::ATOM);
+                            tc::mma_f16_tmem_a(tmem + t * L::TCOLS + L::OCOL, pcol + kk * 8, bd, idO,
+                                               (u > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc::commit(&s_full[sb]);
-                        ++tq;
+                        tc::commit(pv_done(t, u % L::NS));
+                        tc::commit(s_free(t, u % L::NS));
+                        tp[t] = u + 1;
+                        // release the K/V stage once no other tile still needs tile u
+                        const int o = t ^ 1;
+                        if (tp[o] > u || u >= nt_t[o]) tc::commit(&kv_empty[u % L::STAGES]);
                         did = true;
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < L::QT; ++t) {
+                    const int j = tq[t];
+                    if (j < nt_t[t]) {
+                        const int st = j % L::STAGES, sb = j % L::NS;
+                        if (mbar_test(&kv_full[st], (j / L::STAGES) & 1) &&
+                            (j < L::NS || mbar_test(s_free(t, sb), ((j / L::NS) - 1) & 1))) {
+                            tc::fence_after_sync();
+                            const uint32_t kbase = smem_u32(k_tile(st));
+                            const uint32_t qt = qbase + t * L::QTILE;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
+                                const uint32_t koff = (kk >> 2) * L::HALF_OFF + (kk & 3) * 32;
+                                tc::mma_f16(tmem + t * L::TCOLS + sb * 64, tc::sdesc_sw128(qt + off, 16, 1024),
+                                            tc::sdesc_sw128(kbase + koff, 16, L::ATOM), idS, kk > 0 ? 1u : 0u);
+                            }
+                            tc::commit(s_full(t, sb));
+                            tq[t] = j + 1;
+                            did = true;
+                        }
                     }
                 }
                 if (did) {
@@ -255,19 +295,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ============================= softmax ======================================
+        const int t = warp >> 2;                         // query tile of this warpgroup
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                  // row / TMEM lane
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        const int tok = r / G, g = r % G;
+        const uint32_t tbase = tmem + t * L::TCOLS;
+        const int R = t * PM + r;                        // row within the CTA
+        const int tok = R / G, g = R % G;
         const int qi = i0 + tok;
         const bool row_valid = qi < n;
         const int last_key = c + qi;                     // row sees keys 0 .. last_key
+        const int first_key_t = c + i0 + t * L::TOKT;    // smallest last_key in this tile
+        const int nt = nt_t[t];
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < ntiles && ok; ++j) {
+        for (int j = 0; j < nt && ok; ++j) {
             const int sb = j % L::NS;
             const int k0 = j * PN;
-            if (!mbar_wait(&s_full[sb], (j / L::NS) & 1)) {
+            if (!mbar_wait(s_full(t, sb), (j / L::NS) & 1)) {
                 report(p.dev_status, WF_DEV_TIMEOUT);
                 ok = false;
                 break;
@@ -275,13 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             float s[2][32];
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) tc::ld_32cols(tmem + lane_addr + sb * 64 + c2 * 32, s[c2]);
+            for (int c2 = 0; c2 < 2; ++c2) tc::ld_32cols(tbase + lane_addr + sb * 64 + c2 * 32, s[c2]);
             tc::wait_ld();
 
-            // keys some row of the CTA may not see: mask them.  The row max is taken
+            // keys some row of the tile may not see: mask them.  The row max is taken
             // on raw scores (scale > 0) and scaled once.
-            const bool masked = (k0 + PN - 1 > c + i0) || !row_valid;
-            if (masked) {
+            if ((k0 + PN - 1 > first_key_t) || !row_valid) {
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
@@ -311,16 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
                 // O must hold P.V of tile j-1 before it is rescaled
-                if (!mbar_wait(&pv_done[(j - 1) % L::NS], ((j - 1) / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (!mbar_wait(pv_done(t, (j - 1) % L::NS), ((j - 1) / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     float o[32];
-                    tc::ld_32cols(tmem + lane_addr + L::OCOL + c4 * 32, o);
+                    tc::ld_32cols(tbase + lane_addr + L::OCOL + c4 * 32, o);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tc::st_32cols(tmem + lane_addr + L::OCOL + c4 * 32, o);
+                    tc::st_32cols(tbase + lane_addr + L::OCOL + c4 * 32, o);
                 }
                 tc::wait_st();
             }
@@ -345,10 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 pst = __fadd2_rn(ps01, ps23);
             l_run += pst.x + pst.y;
             // P(j) replaces the first 32 S columns of this buffer
-            tc::st_32words(tmem + lane_addr + sb * 64, pw);
+            tc::st_32words(tbase + lane_addr + sb * 64, pw);
             tc::wait_st();
-            // keys past the CTA's end were not loaded (or are stale): zero their V rows.
-            // Thread r owns key r % 64 of the tile and column block r / 64.
+            // keys past the CTA's end were not loaded (or are stale): zero their V rows
+            // (only in the last K/V tile).  Thread r owns key r % 64 and column block
+            // r / 64; when both groups take part in that tile they write the same zeros.
             {
                 const int key = r & 63, cb = r >> 6;
                 if (cb < L::NC && k0 + key >= kend) {
@@ -361,18 +406,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
+            if (lane == 0) mbar_arrive(p_full(t, sb));
         }
         // ---- epilogue: O / l -> bf16 --------------------------------------------------
-        if (ok) {
-            const int last = ntiles - 1;
-            if (!mbar_wait(&pv_done[last % L::NS], (last / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+        if (ok && nt > 0) {
+            const int last = nt - 1;
+            if (!mbar_wait(pv_done(t, last % L::NS), (last / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             tc::fence_after_sync();
             const float inv = row_valid ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 float o[32];
-                tc::ld_32cols(tmem + lane_addr + L::OCOL + c4 * 32, o);
+                tc::ld_32cols(tbase + lane_addr + L::OCOL + c4 * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
                     __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + c4 * 32;
@@ -392,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == kProd) {
+    if (warp == kMma) {
         __syncwarp();
         tc::fence_after_sync();
         tc::dealloc(tmem, L::TMEM_COLS);
