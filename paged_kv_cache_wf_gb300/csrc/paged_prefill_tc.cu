@@ -224,73 +224,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Event loop over two query tiles: O_t += P_t(j) V_j as soon as the weights are
         // ready, else S_t(j) = Q_t K_j^T as soon as tile j has landed and an S buffer
         // of tile t is free.  K/V stage j is released once every tile that uses it is done.
-        if (lane == 0) {
-            constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
-            constexpr uint32_t idO = tc::idesc_bf16_f32(PM, D, 0, 1);
-            bool ok = mbar_wait(q_full, 0);
-            if (!ok) report(p.dev_status, WF_DEV_TIMEOUT);
-            const uint32_t qbase = smem_u32(smem + L::q);
-            int tq[L::QT], tp[L::QT];
+        // The whole warp runs the loop (lane 0's barrier observations decide, broadcast
+        // by shuffle) so that control flow and descriptors stay warp-uniform; lane 0
+        // alone issues.  Descriptors are built once and advanced by adding the byte
+        // offset >> 4 to their start-address field.
+        constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
+        constexpr uint32_t idO = tc::idesc_bf16_f32(PM, D, 0, 1);
+        const bool ok = mbar_wait(q_full, 0);
+        if (!ok && lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+        const uint64_t qdesc = tc::sdesc_sw128(smem_u32(smem + L::q), 16, 1024);
+        const uint64_t kdesc = tc::sdesc_sw128(smem_u32(k_tile(0)), 16, L::ATOM);
+        // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
+        const uint64_t vdesc = tc::sdesc_sw128(smem_u32(v_tile(0)), L::HALF_OFF, L::ATOM);
+        int tq[L::QT], tp[L::QT];
 #pragma unroll
-            for (int t = 0; t < L::QT; ++t) tq[t] = tp[t] = 0;
-            uint32_t idle = 0;
-            while (ok && (tp[0] < nt_t[0] || tp[1] < nt_t[1])) {
-                bool did = false;
+        for (int t = 0; t < L::QT; ++t) tq[t] = tp[t] = 0;
+        uint32_t idle = 0;
+        while (ok && (tp[0] < nt_t[0] || tp[1] < nt_t[1])) {
+            bool did = false;
 #pragma unroll
-                for (int t = 0; t < L::QT; ++t) {
-                    const int u = tp[t];
-                    if (u < tq[t] && mbar_test(p_full(t, u % L::NS), (u / L::NS) & 1)) {
-                        tc::fence_after_sync();
-                        const uint32_t pcol = tmem + t * L::TCOLS + (u % L::NS) * 64;
-                        const uint32_t vbase = smem_u32(v_tile(u % L::STAGES));
+            for (int t = 0; t < L::QT; ++t) {
+                const int u = tp[t];
+                if (u < tq[t] && __shfl_sync(0xffffffffu, (int)mbar_test(p_full(t, u % L::NS), (u / L::NS) & 1), 0)) {
+                    tc::fence_after_sync();
+                    const uint32_t dO = tmem + t * L::TCOLS + L::OCOL;
+                    const uint32_t pcol = tmem + t * L::TCOLS + (u % L::NS) * 64;
+                    const uint64_t vd = vdesc + (uint64_t)(((u % L::STAGES) * L::STAGE) >> 4);
+                    const int o = t ^ 1;
+                    if (lane == 0) {
 #pragma unroll
-                        for (int kk = 0; kk < PN / 16; ++kk) {
-                            // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
-                            const uint64_t bd = tc::sdesc_sw128(vbase + kk * 2 * L::ATOM, L::HALF_OFF, L::ATOM);
-                            tc::mma_f16_tmem_a(tmem + t * L::TCOLS + L::OCOL, pcol + kk * 8, bd, idO,
+                        for (int kk = 0; kk < PN / 16; ++kk)
+                            tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
                                                (u > 0 || kk > 0) ? 1u : 0u);
-                        }
                         tc::commit(pv_done(t, u % L::NS));
                         tc::commit(s_free(t, u % L::NS));
-                        tp[t] = u + 1;
                         // release the K/V stage once no other tile still needs tile u
-                        const int o = t ^ 1;
                         if (tp[o] > u || u >= nt_t[o]) tc::commit(&kv_empty[u % L::STAGES]);
+                    }
+                    __syncwarp();
+                    tp[t] = u + 1;
+                    did = true;
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < L::QT; ++t) {
+                const int j = tq[t];
+                if (j < nt_t[t]) {
+                    const int st = j % L::STAGES, sb = j % L::NS;
+                    const bool rdy = mbar_test(&kv_full[st], (j / L::STAGES) & 1) &&
+                                     (j < L::NS || mbar_test(s_free(t, sb), ((j / L::NS) - 1) & 1));
+                    if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
+                        tc::fence_after_sync();
+                        const uint32_t dS = tmem + t * L::TCOLS + sb * 64;
+                        const uint64_t qd = qdesc + (uint64_t)((t * L::QTILE) >> 4);
+                        const uint64_t kd = kdesc + (uint64_t)((st * L::STAGE) >> 4);
+                        if (lane == 0) {
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t qoff = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
+                                const uint32_t koff = (kk >> 2) * L::HALF_OFF + (kk & 3) * 32;
+                                tc::mma_f16(dS, qd + (uint64_t)(qoff >> 4), kd + (uint64_t)(koff >> 4), idS,
+                                            kk > 0 ? 1u : 0u);
+                            }
+                            tc::commit(s_full(t, sb));
+                        }
+                        __syncwarp();
+                        tq[t] = j + 1;
                         did = true;
                     }
                 }
-#pragma unroll
-                for (int t = 0; t < L::QT; ++t) {
-                    const int j = tq[t];
-                    if (j < nt_t[t]) {
-                        const int st = j % L::STAGES, sb = j % L::NS;
-                        if (mbar_test(&kv_full[st], (j / L::STAGES) & 1) &&
-                            (j < L::NS || mbar_test(s_free(t, sb), ((j / L::NS) - 1) & 1))) {
-                            tc::fence_after_sync();
-                            const uint32_t kbase = smem_u32(k_tile(st));
-                            const uint32_t qt = qbase + t * L::QTILE;
-#pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
-                                const uint32_t koff = (kk >> 2) * L::HALF_OFF + (kk & 3) * 32;
-                                tc::mma_f16(tmem + t * L::TCOLS + sb * 64, tc::sdesc_sw128(qt + off, 16, 1024),
-                                            tc::sdesc_sw128(kbase + koff, 16, L::ATOM), idS, kk > 0 ? 1u : 0u);
-                            }
-                            tc::commit(s_full(t, sb));
-                            tq[t] = j + 1;
-                            did = true;
-                        }
-                    }
+            }
+            if (did) {
+                idle = 0;
+            } else {
+                if (++idle > (1u << 24)) {
+                    if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+                    break;
                 }
-                if (did) {
-                    idle = 0;
-                } else {
-                    if (++idle > (1u << 24)) {
-                        report(p.dev_status, WF_DEV_TIMEOUT);
-                        break;
-                    }
-                    if (idle > 8) __nanosleep(32);
-                }
+                if (idle > 8) __nanosleep(32);
             }
         }
     } else {
