@@ -32,6 +32,8 @@
 //   * A sequence that fits in one split writes its output directly; otherwise each
 //     split leaves (m, l, o) in the workspace and the combine kernel merges them
 //     with a warp-shuffle log-sum-exp reduction.
+#include <type_traits>
+
 #include "wf_internal.h"
 
 namespace wf {
@@ -520,14 +522,20 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, 1) paged_decode_kernel(
 
 // Merge the splits of every (sequence, query head) with more than one split:
 //   out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j.
-// One warp per (b, query head); lanes own D/32 output dims; the split loop keeps
-// several independent loads in flight.
+// One warp per (b, query head); lanes own D/32 output dims.  The merge is bound by
+// the latency of reading the partials, so each lane issues the loads of kBatch
+// splits back to back before using any of them.  Launched as a programmatic
+// dependent of the split kernel: the grid may start while the split kernel drains,
+// and waits for it (griddepcontrol.wait) before reading the workspace.
 template <typename E, int D>
-__global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128, 8) paged_decode_combine_kernel(const DecodeParams p) {
     constexpr int VPL = D / 32;
+    constexpr int kBatch = 8;
+    using Vec = typename std::conditional<VPL == 4, float4, float2>::type;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq = blockIdx.x * 4 + warp;
     const int b = blockIdx.y;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (hq >= p.H_q) return;
     const int len = __ldg(p.seq_lens + b);
     if (!len_ok(len, p)) return;
@@ -550,16 +558,23 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
             den += wl * ml.y;
         }
         const int cnt = min(32, n - j0);
-#pragma unroll 8
-        for (int jj = 0; jj < cnt; ++jj) {
-            const float w = __shfl_sync(0xffffffffu, wl, jj);
-            const float* src = p.ws_o + (base + (int64_t)(j0 + jj) * p.H_q) * D + lane * VPL;
-            if constexpr (VPL == 4) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-                o[0] += w * x.x; o[1] += w * x.y; o[2] += w * x.z; o[3] += w * x.w;
-            } else {
-                const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-                o[0] += w * x.x; o[1] += w * x.y;
+        for (int jj = 0; jj < cnt; jj += kBatch) {
+            Vec x[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (jj + u < cnt)
+                    x[u] = __ldcg(reinterpret_cast<const Vec*>(p.ws_o + (base + (int64_t)(j0 + jj + u) * p.H_q) * D +
+                                                               lane * VPL));
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const float w = __shfl_sync(0xffffffffu, wl, (jj + u) & 31);
+                if (jj + u < cnt) {
+                    if constexpr (VPL == 4) {
+                        o[0] += w * x[u].x; o[1] += w * x[u].y; o[2] += w * x[u].z; o[3] += w * x[u].w;
+                    } else {
+                        o[0] += w * x[u].x; o[1] += w * x[u].y;
+                    }
+                }
             }
         }
     }
@@ -570,6 +585,22 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
     for (int k = 0; k < VPL; ++k) o[k] *= inv;
     char* dst = static_cast<char*>(p.out) + (((int64_t)b * p.H_q + hq) * D + lane * VPL) * E::kBytes;
     store_out<E, VPL>(dst, o);
+}
+
+// The combine kernel as a programmatic dependent launch of the split kernel before it.
+template <typename E, int D>
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.H_q + 3) / 4, p.B);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, paged_decode_combine_kernel<E, D>, p);
 }
 
 int pow2_at_least(int x) {
@@ -606,12 +637,7 @@ cudaError_t launch_typed(DecodeParams& p, cudaStream_t stream) {
     kern<<<grid, (2 * p.HC + 1) * 32, smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    if (p.max_splits > 1) {
-        dim3 cgrid((p.H_q + 3) / 4, p.B);
-        paged_decode_combine_kernel<E, D><<<cgrid, 128, 0, stream>>>(p);
-        err = cudaGetLastError();
-    }
-    return err;
+    return p.max_splits > 1 ? launch_combine<E, D>(p, stream) : cudaSuccess;
 }
 
 template <typename E, int D>
@@ -697,12 +723,7 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
                                                  B, max_seq_len, num_q_heads, scale, pool, p.ws_o, p.ws_ml,
                                                  p.max_splits, dev_status, stream);
         if (err != cudaSuccess) return err;
-        if (p.max_splits > 1) {
-            dim3 cgrid((p.H_q + 3) / 4, p.B);
-            paged_decode_combine_kernel<BF16, 128><<<cgrid, 128, 0, stream>>>(p);
-            err = cudaGetLastError();
-        }
-        return err;
+        return p.max_splits > 1 ? launch_combine<BF16, 128>(p, stream) : cudaSuccess;
     }
     if (pool.dtype == WF_DTYPE_F32) {
         return pool.head_dim == 64 ? launch_group<F32, 64>(p, g.gmax, stream)

@@ -137,6 +137,9 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // the combine grid that follows may be scheduled now; it waits for this grid to
+    // finish before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 1) {
         tc::alloc(tmem_slot, 128);
