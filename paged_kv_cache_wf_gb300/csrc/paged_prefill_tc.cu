@@ -30,8 +30,8 @@ namespace wf {
 
 namespace {
 
-constexpr int PM = 128;          // rows per CTA (TMEM lanes, MMA M)
-constexpr int PN = 64;           // keys per tile
+constexpr int PM = 128;          // rows per query tile (TMEM lanes, MMA M)
+constexpr int PN = 128;          // keys per K/V tile (MMA N of S = Q K^T)
 constexpr float kLazy = 8.f;     // rescale O only when the row max grows by more than 2^8
 // warps 0-7 softmax (two warpgroups, one per query tile), then kProd producer warps,
 // then the MMA warp.  12 warps leave 168 registers per thread.
@@ -51,40 +51,41 @@ struct PfParams {
 };
 
 // One CTA per SM.  Two 128-row query tiles (A, B) share every K/V tile, which
-// doubles the work per loaded byte; each tile has its own softmax warpgroup, its own
-// S/P ring and O accumulator in TMEM, so one group's exponentials overlap the other
-// group's MMAs.  A deep K/V ring covers the ~1 us TMA round trip.
+// doubles the work per loaded byte.  Each query tile has its own softmax
+// warpgroup, S accumulator and O accumulator in TMEM; while one group computes
+// its softmax the tensor core runs the other tile's products.  Every MMA has
+// N >= 128 (S: 128 keys, P.V: N = D), which a single issuing thread keeps fed.
 template <int D, int G>
 struct PfLayout {
     static constexpr int QT = 2;                    // query tiles per CTA
     static constexpr int TOKT = PM / G;             // query tokens per tile
     static constexpr int BMQ = QT * TOKT;           // query tokens per CTA
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
-    static constexpr int STAGES = D == 128 ? 4 : 8; // K/V ring depth
-    static constexpr int TBL = 2048;                // block-table entries staged in shared memory
     static constexpr int QTILE = PM * D * 2;        // one query tile
-    static constexpr int KVHALF = PN * 128;         // one column block of a K or V tile (8 KB)
+    static constexpr int SLOT = PN * D * 2;         // one K or V tile
+    // K/V ring: K(j) is load unit 2j, V(j) unit 2j + 1, unit u in slot u % NSLOT, so a
+    // K tile is released after its S products and a V tile after its P.V products.
+    static constexpr int NSLOT = D == 128 ? 4 : 8;
+    static constexpr int TBL = 2048;                // block-table entries staged in shared memory
     // D = 128: one 4 KB box per 16-key block holds both 64-wide halves, laid out
     // [8-key group][half][8 keys][64 d] -- atoms 2048 B apart, halves 1024 B apart.
     // D = 64: one 2 KB box per block, [16 keys][64 d] -- atoms 1024 B apart.
     static constexpr int ATOM = NC == 2 ? 2048 : 1024;   // stride between 8-key atoms
     static constexpr int HALF_OFF = 1024;                 // offset of the second 64-wide half
     static constexpr int BOX = NC * 2048;                 // bytes of one block's box
-    static constexpr int STAGE = 2 * NC * KVHALF;   // K then V
     static constexpr int q = 0;
     static constexpr int kv = QT * QTILE;
-    static constexpr int tbl = kv + STAGES * STAGE;
+    static constexpr int tbl = kv + NSLOT * SLOT;
     static constexpr int bars = tbl + TBL * 4;
-    static constexpr int NS = 2;                    // S/P buffers per query tile
-    // q_full, kv_full[S], kv_empty[S], then per query tile: s_full[NS], s_free[NS],
-    // p_full[NS], pv_done[NS]
-    static constexpr int nbars = 1 + 2 * STAGES + QT * 4 * NS;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], then per query tile: s_full,
+    // p_full, pv_done
+    static constexpr int nbars = 1 + 2 * NSLOT + QT * 3;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
-    // TMEM per query tile t, base 256 t: S buffers [64 i, 64 i + 64) for i < NS -- P(j)
-    // overwrites the first half of its S buffer -- then O [128, 128 + D).
-    static constexpr int TCOLS = 256;
-    static constexpr int OCOL = NS * 64;
+    // TMEM: S of query tile t in columns [128 t, 128 t + 128) -- its softmax weights
+    // P (bf16 pairs) replace the first 64 of them -- and O of tile t at 256 + D t.
+    static constexpr int SCOL = 128;
+    static constexpr int OCOL = 256;
     static constexpr int TMEM_COLS = 512;
     static_assert(total + 1024 <= 232448, "prefill CTA exceeds shared memory");
 };
@@ -129,17 +130,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
-    uint64_t* kv_empty = kv_full + L::STAGES;
-    uint64_t* tb = kv_empty + L::STAGES;              // per query tile: 4 * NS barriers
-    auto s_full = [&](int t, int i) { return tb + t * 4 * L::NS + i; };
-    auto s_free = [&](int t, int i) { return tb + t * 4 * L::NS + L::NS + i; };
-    auto p_full = [&](int t, int i) { return tb + t * 4 * L::NS + 2 * L::NS + i; };
-    auto pv_done = [&](int t, int i) { return tb + t * 4 * L::NS + 3 * L::NS + i; };
+    uint64_t* slot_full = bars + 1;
+    uint64_t* slot_empty = slot_full + L::NSLOT;
+    uint64_t* tb = slot_empty + L::NSLOT;             // per query tile: s_full, p_full, pv_done
+    auto s_full = [&](int t) { return tb + t * 3; };
+    auto p_full = [&](int t) { return tb + t * 3 + 1; };
+    auto pv_done = [&](int t) { return tb + t * 3 + 2; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::tbl);
-    auto k_tile = [&](int st) { return smem + L::kv + st * L::STAGE; };
-    auto v_tile = [&](int st) { return smem + L::kv + st * L::STAGE + L::NC * L::KVHALF; };
+    // load unit u (K(j): u = 2j, V(j): u = 2j + 1)
+    auto unit_slot = [&](int u) { return smem + L::kv + (u % L::NSLOT) * L::SLOT; };
 
     if (warp == kMma) {
         tc::alloc(tmem_slot, L::TMEM_COLS);
@@ -147,17 +147,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < L::STAGES; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+        for (int i = 0; i < L::NSLOT; ++i) {
+            mbar_init(&slot_full[i], 1);
+            mbar_init(&slot_empty[i], 1);
         }
-        for (int t = 0; t < L::QT; ++t)
-            for (int i = 0; i < L::NS; ++i) {
-                mbar_init(s_full(t, i), 1);
-                mbar_init(s_free(t, i), 1);
-                mbar_init(p_full(t, i), 4);
-                mbar_init(pv_done(t, i), 1);
-            }
+        for (int t = 0; t < L::QT; ++t) {
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), 4);
+            mbar_init(pv_done(t), 1);
+        }
         fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -167,8 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= kSoft && warp < kMma) {
         // ============================= producers ====================================
-        // A thread's TMA copies complete one after another, so consecutive tiles are
-        // issued by different warps (tile j by producer j % kProd) to keep several in flight.
+        // A thread's TMA copies complete one after another, so consecutive load units
+        // are issued by different warps (unit u by producer u % kProd), one 16-key box
+        // per lane, to keep many copies in flight.
         const int pw = warp - kSoft;                     // producer index
         if (pw == 0 && lane == 0) {
             mbar_arrive_expect_tx(q_full, (uint32_t)(L::QT * L::QTILE));
@@ -187,43 +186,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = threadIdx.x - kSoft * 32; i < nblk; i += kProd * 32) tbl[i] = __ldg(trow + i);
             named_bar_sync(2, kProd * 32);
         }
-        for (int j = pw; j < ntiles; j += kProd) {
-            const int st = j % L::STAGES;
+        for (int u = pw; u < 2 * ntiles; u += kProd) {
+            const int j = u >> 1, isv = u & 1;
+            const int sl = u % L::NSLOT;
             const int k0 = j * PN;
             const int kt = min(PN, kend - k0);
-            const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 4)
-            if (j >= L::STAGES && !mbar_wait(&kv_empty[st], ((j / L::STAGES) - 1) & 1)) {
+            const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 8)
+            if (u >= L::NSLOT && !mbar_wait(&slot_empty[sl], ((u / L::NSLOT) - 1) & 1)) {
                 if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
                 break;
             }
-            // one box per lane: lanes 0-3 K of block 0-3, lanes 4-7 V of block 0-3
-            const int bx = lane & 3, isv = (lane >> 2) & 1;
             bool okb = false;
             int blk = 0;
-            if (lane < 8 && bx < nbox) {
-                const int bi = (k0 + bx * 16) / p.P;
+            if (lane < nbox) {
+                const int bi = (k0 + lane * 16) / p.P;
                 blk = staged ? tbl[bi] : __ldg(trow + bi);
                 okb = (unsigned)blk < (unsigned)p.N;
                 if (!okb && isv == 0) report(p.dev_status, WF_DEV_BAD_BLOCK);
             }
             const unsigned okm = __ballot_sync(0xffffffffu, okb);
-            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)__popc(okm) * (uint32_t)L::BOX);
+            if (lane == 0) mbar_arrive_expect_tx(&slot_full[sl], (uint32_t)__popc(okm) * (uint32_t)L::BOX);
             __syncwarp();
             if (okb) {
-                const int slot = blk * p.P + (k0 + bx * 16) % p.P;   // multiple of 16
-                unsigned char* dst = (isv ? v_tile(st) : k_tile(st)) + bx * L::BOX;
+                const int slot = blk * p.P + (k0 + lane * 16) % p.P;   // multiple of 16
+                unsigned char* dst = unit_slot(u) + lane * L::BOX;
                 if constexpr (L::NC == 2) {
-                    tma_load_5d(dst, isv ? &tm_v : &tm_k, 0, 0, 0, slot >> 3, h, &kv_full[st]);
+                    tma_load_5d(dst, isv ? &tm_v : &tm_k, 0, 0, 0, slot >> 3, h, &slot_full[sl]);
                 } else {
-                    tma_load_3d_nohint(dst, isv ? &tm_v : &tm_k, 0, slot, h, &kv_full[st]);
+                    tma_load_3d_nohint(dst, isv ? &tm_v : &tm_k, 0, slot, h, &slot_full[sl]);
                 }
             }
         }
     } else if (warp == kMma) {
         // ============================= MMA issuer ===================================
-        // Event loop over two query tiles: O_t += P_t(j) V_j as soon as the weights are
-        // ready, else S_t(j) = Q_t K_j^T as soon as tile j has landed and an S buffer
-        // of tile t is free.  K/V stage j is released once every tile that uses it is done.
+        // Per query tile t the products run in order S_t(0), P_t(0).V_0, S_t(1), ...:
+        // S_t(j+1) overwrites the columns P_t(j) lives in, and the tensor core executes
+        // one thread's MMAs in issue order.  O_t += P_t(j) V_j is issued as soon as the
+        // softmax has written P_t(j) and V_j has landed; S_t(j+1) = Q_t K_{j+1}^T right
+        // after it once K_{j+1} has landed.  A K or V slot is released by the product
+        // of the last query tile that reads it.
         // The whole warp runs the loop (lane 0's barrier observations decide, broadcast
         // by shuffle) so that control flow and descriptors stay warp-uniform; lane 0
         // alone issues.  Descriptors are built once and advanced by adding the byte
@@ -233,51 +234,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool ok = mbar_wait(q_full, 0);
         if (!ok && lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
         const uint64_t qdesc = tc::sdesc_sw128(smem_u32(smem + L::q), 16, 1024);
-        const uint64_t kdesc = tc::sdesc_sw128(smem_u32(k_tile(0)), 16, L::ATOM);
+        const uint64_t kvdesc_k = tc::sdesc_sw128(smem_u32(smem + L::kv), 16, L::ATOM);
         // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
-        const uint64_t vdesc = tc::sdesc_sw128(smem_u32(v_tile(0)), L::HALF_OFF, L::ATOM);
-        int tq[L::QT], tp[L::QT];
+        const uint64_t kvdesc_v = tc::sdesc_sw128(smem_u32(smem + L::kv), L::HALF_OFF, L::ATOM);
+        int sq[L::QT], sp[L::QT];   // next S and next P.V of each query tile
 #pragma unroll
-        for (int t = 0; t < L::QT; ++t) tq[t] = tp[t] = 0;
+        for (int t = 0; t < L::QT; ++t) sq[t] = sp[t] = 0;
         uint32_t idle = 0;
-        while (ok && (tp[0] < nt_t[0] || tp[1] < nt_t[1])) {
+        while (ok && (sp[0] < nt_t[0] || sp[1] < nt_t[1])) {
             bool did = false;
 #pragma unroll
             for (int t = 0; t < L::QT; ++t) {
-                const int u = tp[t];
-                if (u < tq[t] && __shfl_sync(0xffffffffu, (int)mbar_test(p_full(t, u % L::NS), (u / L::NS) & 1), 0)) {
-                    tc::fence_after_sync();
-                    const uint32_t dO = tmem + t * L::TCOLS + L::OCOL;
-                    const uint32_t pcol = tmem + t * L::TCOLS + (u % L::NS) * 64;
-                    const uint64_t vd = vdesc + (uint64_t)(((u % L::STAGES) * L::STAGE) >> 4);
-                    const int o = t ^ 1;
-                    if (lane == 0) {
-#pragma unroll
-                        for (int kk = 0; kk < PN / 16; ++kk)
-                            tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
-                                               (u > 0 || kk > 0) ? 1u : 0u);
-                        tc::commit(pv_done(t, u % L::NS));
-                        tc::commit(s_free(t, u % L::NS));
-                        // release the K/V stage once no other tile still needs tile u
-                        if (tp[o] > u || u >= nt_t[o]) tc::commit(&kv_empty[u % L::STAGES]);
-                    }
-                    __syncwarp();
-                    tp[t] = u + 1;
-                    did = true;
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < L::QT; ++t) {
-                const int j = tq[t];
-                if (j < nt_t[t]) {
-                    const int st = j % L::STAGES, sb = j % L::NS;
-                    const bool rdy = mbar_test(&kv_full[st], (j / L::STAGES) & 1) &&
-                                     (j < L::NS || mbar_test(s_free(t, sb), ((j / L::NS) - 1) & 1));
+                const int o = t ^ 1;
+                const int u = sp[t];
+                if (u < sq[t]) {
+                    const int vu = 2 * u + 1;
+                    const bool rdy = mbar_test(p_full(t), u & 1) &&
+                                     mbar_test(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1);
                     if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
                         tc::fence_after_sync();
-                        const uint32_t dS = tmem + t * L::TCOLS + sb * 64;
+                        const uint32_t dO = tmem + L::OCOL + t * D;
+                        const uint32_t pcol = tmem + t * L::SCOL;
+                        const uint64_t vd = kvdesc_v + (uint64_t)(((vu % L::NSLOT) * L::SLOT) >> 4);
+                        if (lane == 0) {
+#pragma unroll
+                            for (int kk = 0; kk < PN / 16; ++kk)
+                                tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
+                                                   (u > 0 || kk > 0) ? 1u : 0u);
+                            tc::commit(pv_done(t));
+                            if (sp[o] > u || u >= nt_t[o]) tc::commit(&slot_empty[vu % L::NSLOT]);
+                        }
+                        __syncwarp();
+                        sp[t] = u + 1;
+                        did = true;
+                    }
+                }
+                const int j = sq[t];
+                if (j < nt_t[t] && j == sp[t]) {
+                    const int ku = 2 * j;
+                    const bool rdy = mbar_test(&slot_full[ku % L::NSLOT], (ku / L::NSLOT) & 1);
+                    if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
+                        tc::fence_after_sync();
+                        const uint32_t dS = tmem + t * L::SCOL;
                         const uint64_t qd = qdesc + (uint64_t)((t * L::QTILE) >> 4);
-                        const uint64_t kd = kdesc + (uint64_t)((st * L::STAGE) >> 4);
+                        const uint64_t kd = kvdesc_k + (uint64_t)(((ku % L::NSLOT) * L::SLOT) >> 4);
                         if (lane == 0) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
@@ -286,10 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tc::mma_f16(dS, qd + (uint64_t)(qoff >> 4), kd + (uint64_t)(koff >> 4), idS,
                                             kk > 0 ? 1u : 0u);
                             }
-                            tc::commit(s_full(t, sb));
+                            tc::commit(s_full(t));
+                            if (sq[o] > j || j >= nt_t[o]) tc::commit(&slot_empty[ku % L::NSLOT]);
                         }
                         __syncwarp();
-                        tq[t] = j + 1;
+                        sq[t] = j + 1;
                         did = true;
                     }
                 }
@@ -310,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                  // row / TMEM lane
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        const uint32_t tbase = tmem + t * L::TCOLS;
+        const uint32_t sbase = tmem + lane_addr + t * L::SCOL;
+        const uint32_t obase = tmem + lane_addr + L::OCOL + t * D;
         const int R = t * PM + r;                        // row within the CTA
         const int tok = R / G, g = R % G;
         const int qi = i0 + tok;
@@ -321,38 +323,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < nt && ok; ++j) {
-            const int sb = j % L::NS;
             const int k0 = j * PN;
-            if (!mbar_wait(s_full(t, sb), (j / L::NS) & 1)) {
+            if (!mbar_wait(s_full(t), j & 1)) {
                 report(p.dev_status, WF_DEV_TIMEOUT);
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            float s[2][32];
+            // keys some row of the tile may not see are masked.  The row max is taken on
+            // raw scores (scale > 0) and scaled once.  Two passes over S in 64-column
+            // halves: the maximum, then the weights.
+            const bool masked = (k0 + PN - 1 > first_key_t) || !row_valid;
+            float m8[8];
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) tc::ld_32cols(tbase + lane_addr + sb * 64 + c2 * 32, s[c2]);
-            tc::wait_ld();
-
-            // keys some row of the tile may not see: mask them.  The row max is taken
-            // on raw scores (scale > 0) and scaled once.
-            if ((k0 + PN - 1 > first_key_t) || !row_valid) {
+            for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float s[2][32];
+                tc::ld_32cols(sbase + hh * 64, s[0]);
+                tc::ld_32cols(sbase + hh * 64 + 32, s[1]);
+                tc::wait_ld();
+                if (masked) {
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const bool vis = row_valid && k0 + hh * 64 + c2 * 32 + e <= last_key;
+                            s[c2][e] = vis ? s[c2][e] : -INFINITY;
+                        }
+                }
+                // 8 independent running maxima (short dependency chains)
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const bool vis = row_valid && k0 + c2 * 32 + e <= last_key;
-                        s[c2][e] = vis ? s[c2][e] : -INFINITY;
-                    }
+                    for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[c2][e]);
             }
-            // tree of 8 independent running maxima (short dependency chains)
-            float m8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = fmaxf(s[0][e], s[1][e]);
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2)
-#pragma unroll
-                for (int e = 8; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[c2][e]);
             const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                      fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float mt = mraw * p.scale_log2;
@@ -366,16 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
                 // O must hold P.V of tile j-1 before it is rescaled
-                if (!mbar_wait(pv_done(t, (j - 1) % L::NS), ((j - 1) / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (!mbar_wait(pv_done(t), (j - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     float o[32];
-                    tc::ld_32cols(tbase + lane_addr + L::OCOL + c4 * 32, o);
+                    tc::ld_32cols(obase + c4 * 32, o);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tc::st_32cols(tbase + lane_addr + L::OCOL + c4 * 32, o);
+                    tc::st_32cols(obase + c4 * 32, o);
                 }
                 tc::wait_st();
             }
@@ -385,50 +390,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 nm2 = make_float2(-m_use, -m_use);
             float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
-            uint32_t pw[32];  // keys 2k, 2k+1 of the tile as a bf16 pair
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pw[32];  // keys 2k, 2k+1 of this half as a bf16 pair
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2)
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    float s[32];
+                    tc::ld_32cols(sbase + hh * 64 + c2 * 32, s);
+                    tc::wait_ld();
+                    if (masked) {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
-                    const float2 x = __ffma2_rn(make_float2(s[c2][2 * u], s[c2][2 * u + 1]), sc2, nm2);
-                    const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
-                    ps[u & 3] = __fadd2_rn(ps[u & 3], e2);
-                    pw[c2 * 16 + u] = pack_bf16x2(e2.x, e2.y);
+                        for (int e = 0; e < 32; ++e) {
+                            const bool vis = row_valid && k0 + hh * 64 + c2 * 32 + e <= last_key;
+                            s[e] = vis ? s[e] : -INFINITY;
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
+                        const float2 x = __ffma2_rn(make_float2(s[2 * u], s[2 * u + 1]), sc2, nm2);
+                        const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
+                        ps[u & 3] = __fadd2_rn(ps[u & 3], e2);
+                        pw[c2 * 16 + u] = pack_bf16x2(e2.x, e2.y);
+                    }
                 }
+                // P of keys [64 hh, 64 hh + 64) into columns [32 hh, 32 hh + 32): S there
+                // has been read already
+                tc::st_32words(sbase + hh * 32, pw);
+            }
+            tc::wait_st();
             const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
             const float2 pst = __fadd2_rn(ps01, ps23);
             l_run += pst.x + pst.y;
-            // P(j) replaces the first 32 S columns of this buffer
-            tc::st_32words(tbase + lane_addr + sb * 64, pw);
-            tc::wait_st();
-            // keys past the CTA's end were not loaded (or are stale): zero their V rows
-            // (only in the last K/V tile).  Thread r owns key r % 64 and column block
-            // r / 64; when both groups take part in that tile they write the same zeros.
-            {
-                const int key = r & 63, cb = r >> 6;
-                if (cb < L::NC && k0 + key >= kend) {
-                    uint4* row = reinterpret_cast<uint4*>(v_tile(j % L::STAGES) + (key >> 3) * L::ATOM +
-                                                          cb * L::HALF_OFF + (key & 7) * 128);
+            if (k0 + PN > kend) {
+                // keys past the CTA's end were not loaded (or are stale): zero their V
+                // rows once V_j has landed.  Thread r owns key r; when both groups take
+                // part in this last tile they write the same zeros.
+                const int vu = 2 * j + 1;
+                if (!mbar_wait(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (k0 + r >= kend) {
 #pragma unroll
-                    for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int cb = 0; cb < L::NC; ++cb) {
+                        uint4* row = reinterpret_cast<uint4*>(unit_slot(vu) + (r >> 3) * L::ATOM +
+                                                              cb * L::HALF_OFF + (r & 7) * 128);
+#pragma unroll
+                        for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
+                tc::fence_proxy_async_smem();
             }
-            tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(t, sb));
+            if (lane == 0) mbar_arrive(p_full(t));
         }
         // ---- epilogue: O / l -> bf16 --------------------------------------------------
         if (ok && nt > 0) {
-            const int last = nt - 1;
-            if (!mbar_wait(pv_done(t, last % L::NS), (last / L::NS) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+            if (!mbar_wait(pv_done(t), (nt - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             tc::fence_after_sync();
             const float inv = row_valid ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 float o[32];
-                tc::ld_32cols(tbase + lane_addr + L::OCOL + c4 * 32, o);
+                tc::ld_32cols(obase + c4 * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
                     __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + c4 * 32;
