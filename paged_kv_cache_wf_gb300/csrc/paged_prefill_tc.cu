@@ -36,7 +36,7 @@ constexpr float kLazy = 8.f;     // rescale O only when the row max grows by mor
 // warps 0-7 softmax (two warpgroups, one per query tile), then kProd producer warps,
 // then the MMA warp.  12 warps leave 168 registers per thread.
 constexpr int kSoft = 8;
-constexpr int kProd = 3;         // producer warps: tile j is issued by producer j % kProd
+constexpr int kProd = 3;         // producer warps: ring slot s is refilled by producer s % kProd
 constexpr int kMma = kSoft + kProd;
 constexpr int kThreads = (kMma + 1) * 32;
 
@@ -63,10 +63,13 @@ struct PfLayout {
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
     static constexpr int QTILE = PM * D * 2;        // one query tile
     static constexpr int SLOT = PN * D * 2;         // one K or V tile
-    // K/V ring: K(j) is load unit 2j, V(j) unit 2j + 1, unit u in slot u % NSLOT, so a
-    // K tile is released after its S products and a V tile after its P.V products.
-    static constexpr int NSLOT = D == 128 ? 4 : 8;
-    static constexpr int TBL = 2048;                // block-table entries staged in shared memory
+    // Two rings: K(j) in K slot j % NK, V(j) in V slot j % NV.  A K tile is released
+    // after its S products, a V tile only after its P.V products (a tile later), so V
+    // gets the deeper ring.  Load unit u = 2j + (0 for K, 1 for V).
+    static constexpr int NK = D == 128 ? 2 : 4;
+    static constexpr int NV = D == 128 ? 3 : 6;
+    static constexpr int NSLOT = NK + NV;
+    static constexpr int TBL = D == 128 ? 256 : 2048;   // block-table entries staged in shared memory
     // D = 128: one 4 KB box per 16-key block holds both 64-wide halves, laid out
     // [8-key group][half][8 keys][64 d] -- atoms 2048 B apart, halves 1024 B apart.
     // D = 64: one 2 KB box per block, [16 keys][64 d] -- atoms 1024 B apart.
@@ -77,8 +80,8 @@ struct PfLayout {
     static constexpr int kv = QT * QTILE;
     static constexpr int tbl = kv + NSLOT * SLOT;
     static constexpr int bars = tbl + TBL * 4;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT], then per query tile: s_full,
-    // p_full, pv_done
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT] (K slots, then V slots), then per
+    // query tile: s_full, p_full, pv_done
     static constexpr int nbars = 1 + 2 * NSLOT + QT * 3;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
@@ -138,8 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pv_done = [&](int t) { return tb + t * 3 + 2; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::tbl);
-    // load unit u (K(j): u = 2j, V(j): u = 2j + 1)
-    auto unit_slot = [&](int u) { return smem + L::kv + (u % L::NSLOT) * L::SLOT; };
+    // ring slot of load unit u (K(j): u = 2j, V(j): u = 2j + 1), and the phase of that
+    // slot's barriers the unit uses
+    auto slot_of = [&](int u) { return (u & 1) ? L::NK + (u >> 1) % L::NV : (u >> 1) % L::NK; };
+    auto round_of = [&](int u) { return (u & 1) ? (u >> 1) / L::NV : (u >> 1) / L::NK; };
+    auto unit_slot = [&](int u) { return smem + L::kv + slot_of(u) * L::SLOT; };
 
     if (warp == kMma) {
         tc::alloc(tmem_slot, L::TMEM_COLS);
@@ -165,9 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= kSoft && warp < kMma) {
         // ============================= producers ====================================
-        // A thread's TMA copies complete one after another, so consecutive load units
-        // are issued by different warps (unit u by producer u % kProd), one 16-key box
-        // per lane, to keep many copies in flight.
+        // A thread's TMA copies complete one after another, so the load units are spread
+        // over several warps, one 16-key box per lane, to keep many copies in flight.
         const int pw = warp - kSoft;                     // producer index
         if (pw == 0 && lane == 0) {
             mbar_arrive_expect_tx(q_full, (uint32_t)(L::QT * L::QTILE));
@@ -186,13 +191,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = threadIdx.x - kSoft * 32; i < nblk; i += kProd * 32) tbl[i] = __ldg(trow + i);
             named_bar_sync(2, kProd * 32);
         }
-        for (int u = pw; u < 2 * ntiles; u += kProd) {
+        // Each ring slot is refilled by one producer warp (slot s by producer s % kProd),
+        // in order: a parity wait tells phase r from phase r - 2 only if the waiter is at
+        // most one phase ahead, so no warp may move on to a slot's next round before the
+        // previous one was issued.  A warp takes its units in increasing order.
+        for (int u = 0; u < 2 * ntiles; ++u) {
             const int j = u >> 1, isv = u & 1;
-            const int sl = u % L::NSLOT;
+            const int sl = slot_of(u), rd = round_of(u);
+            if (sl % kProd != pw) continue;
             const int k0 = j * PN;
             const int kt = min(PN, kend - k0);
             const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 8)
-            if (u >= L::NSLOT && !mbar_wait(&slot_empty[sl], ((u / L::NSLOT) - 1) & 1)) {
+            if (rd > 0 && !mbar_wait(&slot_empty[sl], (rd - 1) & 1)) {
                 if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
                 break;
             }
@@ -243,26 +253,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t idle = 0;
         while (ok && (sp[0] < nt_t[0] || sp[1] < nt_t[1])) {
             bool did = false;
+            // the query tile that is behind goes first: both must finish with a V tile
+            // before its slot can be refilled
+            const int first = (sp[1] < sp[0] && sp[1] < nt_t[1]) ? 1 : 0;
 #pragma unroll
-            for (int t = 0; t < L::QT; ++t) {
+            for (int tt = 0; tt < L::QT; ++tt) {
+                const int t = tt ^ first;
                 const int o = t ^ 1;
                 const int u = sp[t];
                 if (u < sq[t]) {
                     const int vu = 2 * u + 1;
                     const bool rdy = mbar_test(p_full(t), u & 1) &&
-                                     mbar_test(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1);
+                                     mbar_test(&slot_full[slot_of(vu)], round_of(vu) & 1);
                     if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
                         tc::fence_after_sync();
                         const uint32_t dO = tmem + L::OCOL + t * D;
                         const uint32_t pcol = tmem + t * L::SCOL;
-                        const uint64_t vd = kvdesc_v + (uint64_t)(((vu % L::NSLOT) * L::SLOT) >> 4);
+                        const uint64_t vd = kvdesc_v + (uint64_t)((slot_of(vu) * L::SLOT) >> 4);
                         if (lane == 0) {
 #pragma unroll
                             for (int kk = 0; kk < PN / 16; ++kk)
                                 tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
                                                    (u > 0 || kk > 0) ? 1u : 0u);
                             tc::commit(pv_done(t));
-                            if (sp[o] > u || u >= nt_t[o]) tc::commit(&slot_empty[vu % L::NSLOT]);
+                            if (sp[o] > u || u >= nt_t[o]) tc::commit(&slot_empty[slot_of(vu)]);
                         }
                         __syncwarp();
                         sp[t] = u + 1;
@@ -272,12 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = sq[t];
                 if (j < nt_t[t] && j == sp[t]) {
                     const int ku = 2 * j;
-                    const bool rdy = mbar_test(&slot_full[ku % L::NSLOT], (ku / L::NSLOT) & 1);
+                    const bool rdy = mbar_test(&slot_full[slot_of(ku)], round_of(ku) & 1);
                     if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
                         tc::fence_after_sync();
                         const uint32_t dS = tmem + t * L::SCOL;
                         const uint64_t qd = qdesc + (uint64_t)((t * L::QTILE) >> 4);
-                        const uint64_t kd = kvdesc_k + (uint64_t)(((ku % L::NSLOT) * L::SLOT) >> 4);
+                        const uint64_t kd = kvdesc_k + (uint64_t)((slot_of(ku) * L::SLOT) >> 4);
                         if (lane == 0) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             kk > 0 ? 1u : 0u);
                             }
                             tc::commit(s_full(t));
-                            if (sq[o] > j || j >= nt_t[o]) tc::commit(&slot_empty[ku % L::NSLOT]);
+                            if (sq[o] > j || j >= nt_t[o]) tc::commit(&slot_empty[slot_of(ku)]);
                         }
                         __syncwarp();
                         sq[t] = j + 1;
@@ -427,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // rows once V_j has landed.  Thread r owns key r; when both groups take
                 // part in this last tile they write the same zeros.
                 const int vu = 2 * j + 1;
-                if (!mbar_wait(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (!mbar_wait(&slot_full[slot_of(vu)], round_of(vu) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
                 if (k0 + r >= kend) {
 #pragma unroll
                     for (int cb = 0; cb < L::NC; ++cb) {
