@@ -63,13 +63,10 @@ struct PfLayout {
     static constexpr int NC = D / 64;               // 64-wide column blocks of D
     static constexpr int QTILE = PM * D * 2;        // one query tile
     static constexpr int SLOT = PN * D * 2;         // one K or V tile
-    // Two rings: K(j) in K slot j % NK, V(j) in V slot j % NV.  A K tile is released
-    // after its S products, a V tile only after its P.V products (a tile later), so V
-    // gets the deeper ring.  Load unit u = 2j + (0 for K, 1 for V).
-    static constexpr int NK = D == 128 ? 2 : 4;
-    static constexpr int NV = D == 128 ? 3 : 6;
-    static constexpr int NSLOT = NK + NV;
-    static constexpr int TBL = D == 128 ? 256 : 2048;   // block-table entries staged in shared memory
+    // K/V ring: K(j) is load unit 2j, V(j) unit 2j + 1, unit u in slot u % NSLOT, so a
+    // K tile is released after its S products and a V tile after its P.V products.
+    static constexpr int NSLOT = D == 128 ? 4 : 8;
+    static constexpr int TBL = 2048;                // block-table entries staged in shared memory
     // D = 128: one 4 KB box per 16-key block holds both 64-wide halves, laid out
     // [8-key group][half][8 keys][64 d] -- atoms 2048 B apart, halves 1024 B apart.
     // D = 64: one 2 KB box per block, [16 keys][64 d] -- atoms 1024 B apart.
@@ -80,8 +77,8 @@ struct PfLayout {
     static constexpr int kv = QT * QTILE;
     static constexpr int tbl = kv + NSLOT * SLOT;
     static constexpr int bars = tbl + TBL * 4;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT] (K slots, then V slots), then per
-    // query tile: s_full, p_full, pv_done
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], then per query tile: s_full,
+    // p_full, pv_done
     static constexpr int nbars = 1 + 2 * NSLOT + QT * 3;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
@@ -141,11 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pv_done = [&](int t) { return tb + t * 3 + 2; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::tbl);
-    // ring slot of load unit u (K(j): u = 2j, V(j): u = 2j + 1), and the phase of that
-    // slot's barriers the unit uses
-    auto slot_of = [&](int u) { return (u & 1) ? L::NK + (u >> 1) % L::NV : (u >> 1) % L::NK; };
-    auto round_of = [&](int u) { return (u & 1) ? (u >> 1) / L::NV : (u >> 1) / L::NK; };
-    auto unit_slot = [&](int u) { return smem + L::kv + slot_of(u) * L::SLOT; };
+    // load unit u (K(j): u = 2j, V(j): u = 2j + 1)
+    auto unit_slot = [&](int u) { return smem + L::kv + (u % L::NSLOT) * L::SLOT; };
 
     if (warp == kMma) {
         tc::alloc(tmem_slot, L::TMEM_COLS);
@@ -197,12 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // previous one was issued.  A warp takes its units in increasing order.
         for (int u = 0; u < 2 * ntiles; ++u) {
             const int j = u >> 1, isv = u & 1;
-            const int sl = slot_of(u), rd = round_of(u);
+            const int sl = u % L::NSLOT;
             if (sl % kProd != pw) continue;
             const int k0 = j * PN;
             const int kt = min(PN, kend - k0);
             const int nbox = (kt + 15) >> 4;            // 16-key blocks in this tile (<= 8)
-            if (rd > 0 && !mbar_wait(&slot_empty[sl], (rd - 1) & 1)) {
+            if (u >= L::NSLOT && !mbar_wait(&slot_empty[sl], ((u / L::NSLOT) - 1) & 1)) {
                 if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
                 break;
             }
@@ -253,30 +247,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t idle = 0;
         while (ok && (sp[0] < nt_t[0] || sp[1] < nt_t[1])) {
             bool did = false;
-            // the query tile that is behind goes first: both must finish with a V tile
-            // before its slot can be refilled
-            const int first = (sp[1] < sp[0] && sp[1] < nt_t[1]) ? 1 : 0;
 #pragma unroll
-            for (int tt = 0; tt < L::QT; ++tt) {
-                const int t = tt ^ first;
+            for (int t = 0; t < L::QT; ++t) {
                 const int o = t ^ 1;
                 const int u = sp[t];
                 if (u < sq[t]) {
                     const int vu = 2 * u + 1;
                     const bool rdy = mbar_test(p_full(t), u & 1) &&
-                                     mbar_test(&slot_full[slot_of(vu)], round_of(vu) & 1);
+                                     mbar_test(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1);
                     if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
                         tc::fence_after_sync();
                         const uint32_t dO = tmem + L::OCOL + t * D;
                         const uint32_t pcol = tmem + t * L::SCOL;
-                        const uint64_t vd = kvdesc_v + (uint64_t)((slot_of(vu) * L::SLOT) >> 4);
+                        const uint64_t vd = kvdesc_v + (uint64_t)(((vu % L::NSLOT) * L::SLOT) >> 4);
                         if (lane == 0) {
 #pragma unroll
                             for (int kk = 0; kk < PN / 16; ++kk)
                                 tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
                                                    (u > 0 || kk > 0) ? 1u : 0u);
                             tc::commit(pv_done(t));
-                            if (sp[o] > u || u >= nt_t[o]) tc::commit(&slot_empty[slot_of(vu)]);
+                            if (sp[o] > u || u >= nt_t[o]) tc::commit(&slot_empty[vu % L::NSLOT]);
                         }
                         __syncwarp();
                         sp[t] = u + 1;
@@ -286,12 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = sq[t];
                 if (j < nt_t[t] && j == sp[t]) {
                     const int ku = 2 * j;
-                    const bool rdy = mbar_test(&slot_full[slot_of(ku)], round_of(ku) & 1);
+                    const bool rdy = mbar_test(&slot_full[ku % L::NSLOT], (ku / L::NSLOT) & 1);
                     if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
                         tc::fence_after_sync();
                         const uint32_t dS = tmem + t * L::SCOL;
                         const uint64_t qd = qdesc + (uint64_t)((t * L::QTILE) >> 4);
-                        const uint64_t kd = kvdesc_k + (uint64_t)((slot_of(ku) * L::SLOT) >> 4);
+                        const uint64_t kd = kvdesc_k + (uint64_t)(((ku % L::NSLOT) * L::SLOT) >> 4);
                         if (lane == 0) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
@@ -301,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             kk > 0 ? 1u : 0u);
                             }
                             tc::commit(s_full(t));
-                            if (sq[o] > j || j >= nt_t[o]) tc::commit(&slot_empty[slot_of(ku)]);
+                            if (sq[o] > j || j >= nt_t[o]) tc::commit(&slot_empty[ku % L::NSLOT]);
                         }
                         __syncwarp();
                         sq[t] = j + 1;
@@ -366,11 +356,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             s[c2][e] = vis ? s[c2][e] : -INFINITY;
                         }
                 }
-                // 8 independent running maxima (short dependency chains)
+                // 8 independent running maxima (short dependency chains), two inputs a step
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[c2][e]);
+                    for (int e = 0; e < 16; ++e) m8[e & 7] = fmax3(m8[e & 7], s[c2][e], s[c2][e + 16]);
             }
             const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                      fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -441,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // rows once V_j has landed.  Thread r owns key r; when both groups take
                 // part in this last tile they write the same zeros.
                 const int vu = 2 * j + 1;
-                if (!mbar_wait(&slot_full[slot_of(vu)], round_of(vu) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (!mbar_wait(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
                 if (k0 + r >= kend) {
 #pragma unroll
                     for (int cb = 0; cb < L::NC; ++cb) {
