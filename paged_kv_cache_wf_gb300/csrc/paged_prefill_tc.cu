@@ -7,21 +7,24 @@
 // [N, P, H_kv, D] pool through block_table[b][p / P], offset p % P (ember, "The core
 // idea"); query head g uses KV head g / G (weft, "Shapes and symbols").
 //
-// GB300 design.  One CTA = one request, one KV head and 128 rows r = (token, g):
-// 128/G consecutive query tokens times the G query heads that share the KV head, so
-// every K/V tile serves the whole group.
-//   warp 0   producer: TMA loads of the Q tile (3D box d x head x token) and, tile by
-//            tile, of 128 keys of K and V gathered block by block through the table
-//            (16-slot boxes, 128-byte swizzle, several issuing lanes) into a 2-stage ring.
-//   warp 1   MMA issuer, event loop: S(j) = Q K_j^T into one of two TMEM S buffers
-//            (M=128 rows, N=128 keys, K=D) as soon as tile j has landed, and
-//            O += P(j) V_j (M=128, N=D, K=128 keys, V read MN-major) as soon as the
-//            softmax has written P(j); commits release stages and buffers.
-//   warps 2-5  softmax, thread r <-> row r <-> TMEM lane r: causal mask (only on
-//            tiles that cross the diagonal), online softmax in the exp2 domain with a
-//            lazy rescale (O in TMEM is rescaled only when a row max grows by more than
-//            2^8, so almost never), P written as bf16 into a swizzled shared tile; the
-//            epilogue divides O by the row sum.
+// GB300 design.  One CTA = one request, one KV head and two query tiles of 128
+// rows r = (token, g): 128/G consecutive query tokens times the G query heads that
+// share the KV head.  Every 128-key K/V tile loaded serves both query tiles (256
+// rows), and every MMA has N >= 128.  12 warps:
+//   warps 0-7   softmax, one warpgroup per query tile; thread r <-> row r <-> TMEM
+//               lane r: causal mask (only on tiles that cross the diagonal), online
+//               softmax in the exp2 domain with a lazy rescale (O in TMEM is rescaled
+//               only when a row max grows by more than 2^8), P written as bf16 pairs
+//               over the first half of the tile's S columns in TMEM; the epilogue
+//               divides O by the row sum.
+//   warps 8-10  producers: TMA loads of the two Q tiles (3D box d x head x token) and,
+//               tile by tile, of 128 keys of K and V gathered 16-key block by block
+//               through the block table (one box per lane, 128-byte swizzle) into a
+//               ring of K and V slots.
+//   warp 11     MMA issuer, event loop over both query tiles: S_t(j) = Q_t K_j^T
+//               (M=128, N=128 keys, K=D) into TMEM, O_t += P_t(j) V_j (M=128, N=D,
+//               K=128 keys, P from TMEM, V MN-major from shared memory); commits hand
+//               S to the softmax and release ring slots.
 #include <cuda.h>
 
 #include "wf_internal.h"
@@ -79,13 +82,9 @@ struct PfLayout {
     static constexpr int bars = tbl + TBL * 4;
     // q_full, slot_full[NSLOT], slot_empty[NSLOT], then per query tile: s_full,
     // p_full, pv_done
-    static constexpr int nbars = 1 + 2 * NSLOT + QT * 3 + 4;   // + one per pair of softmax warps
+    static constexpr int nbars = 1 + 2 * NSLOT + QT * 3;
     static constexpr int tmem_slot = bars + nbars * 8;
-    // row maxima exchanged by the two warps that share a row ([tile parity][half][row])
-    // and row sums for the epilogue ([query tile][half][row])
-    static constexpr int xmax = tmem_slot + 16;
-    static constexpr int xsum = xmax + 2 * 2 * PM * 4;
-    static constexpr int total = xsum + 2 * 2 * PM * 4;
+    static constexpr int total = tmem_slot + 16;
     // TMEM: S of query tile t in columns [128 t, 128 t + 128) -- its softmax weights
     // P (bf16 pairs) replace the first 64 of them -- and O of tile t at 256 + D t.
     static constexpr int SCOL = 128;
@@ -140,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto s_full = [&](int t) { return tb + t * 3; };
     auto p_full = [&](int t) { return tb + t * 3 + 1; };
     auto pv_done = [&](int t) { return tb + t * 3 + 2; };
-    uint64_t* pair_bars = tb + L::QT * 3;             // [4]: softmax warps q and q + 4
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::tbl);
     // load unit u (K(j): u = 2j, V(j): u = 2j + 1)
@@ -158,10 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < L::QT; ++t) {
             mbar_init(s_full(t), 1);
-            mbar_init(p_full(t), 8);
+            mbar_init(p_full(t), 4);
             mbar_init(pv_done(t), 1);
         }
-        for (int q = 0; q < 4; ++q) mbar_init(&pair_bars[q], 2);
         fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -189,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool staged = nblk <= L::TBL;
         if (staged) {
             for (int i = threadIdx.x - kSoft * 32; i < nblk; i += kProd * 32) tbl[i] = __ldg(trow + i);
-            named_bar_sync(5, kProd * 32);
+            named_bar_sync(2, kProd * 32);
         }
         // Each ring slot is refilled by one producer warp (slot s by producer s % kProd),
         // in order: a parity wait tells phase r from phase r - 2 only if the waiter is at
@@ -229,254 +226,242 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMma) {
         // ============================= MMA issuer ===================================
-        // Fixed order: S_0(0), S_1(0), then for each K/V tile j and query tile t:
-        // O_t += P_t(j) V_j once the softmax has written P_t(j), then S_t(j+1) =
-        // Q_t K_{j+1}^T.  S_t(j+1) overwrites the columns P_t(j) lives in; the tensor
-        // core executes one thread's MMAs in issue order.  While the softmax warps work
-        // on one query tile, the tensor core runs the other tile's two products.  A K or
-        // V slot is released by the product of the last query tile that reads it.
-        // The whole warp waits (lane 0 issues), so control flow stays warp-uniform;
-        // descriptors are built once and advanced by adding the byte offset >> 4 to
-        // their start-address field.
+        // Per query tile t the products run in order S_t(0), P_t(0).V_0, S_t(1), ...:
+        // S_t(j+1) overwrites the columns P_t(j) lives in, and the tensor core executes
+        // one thread's MMAs in issue order.  O_t += P_t(j) V_j is issued as soon as the
+        // softmax has written P_t(j) and V_j has landed; S_t(j+1) = Q_t K_{j+1}^T right
+        // after it once K_{j+1} has landed.  A K or V slot is released by the product
+        // of the last query tile that reads it.
+        // The whole warp runs the loop (lane 0's barrier observations decide, broadcast
+        // by shuffle) so that control flow and descriptors stay warp-uniform; lane 0
+        // alone issues.  Descriptors are built once and advanced by adding the byte
+        // offset >> 4 to their start-address field.
         constexpr uint32_t idS = tc::idesc_bf16_f32(PM, PN, 0, 0);
         constexpr uint32_t idO = tc::idesc_bf16_f32(PM, D, 0, 1);
-        bool ok = mbar_wait(q_full, 0);
+        const bool ok = mbar_wait(q_full, 0);
+        if (!ok && lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
         const uint64_t qdesc = tc::sdesc_sw128(smem_u32(smem + L::q), 16, 1024);
         const uint64_t kvdesc_k = tc::sdesc_sw128(smem_u32(smem + L::kv), 16, L::ATOM);
         // V as MN-major B: 64-wide halves HALF_OFF apart, 8-key atoms ATOM apart
         const uint64_t kvdesc_v = tc::sdesc_sw128(smem_u32(smem + L::kv), L::HALF_OFF, L::ATOM);
-        auto last_user = [&](int t, int j) { return t == 1 || j >= nt_t[1]; };
-        auto issue_s = [&](int t, int j) {
-            const int ku = 2 * j;
-            if (!mbar_wait(&slot_full[ku % L::NSLOT], (ku / L::NSLOT) & 1)) return false;
-            tc::fence_after_sync();
-            const uint32_t dS = tmem + t * L::SCOL;
-            const uint64_t qd = qdesc + (uint64_t)((t * L::QTILE) >> 4);
-            const uint64_t kd = kvdesc_k + (uint64_t)(((ku % L::NSLOT) * L::SLOT) >> 4);
-            if (lane == 0) {
+        int sq[L::QT], sp[L::QT];   // next S and next P.V of each query tile
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qoff = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
-                    const uint32_t koff = (kk >> 2) * L::HALF_OFF + (kk & 3) * 32;
-                    tc::mma_f16(dS, qd + (uint64_t)(qoff >> 4), kd + (uint64_t)(koff >> 4), idS, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(s_full(t));
-                if (last_user(t, j)) tc::commit(&slot_empty[ku % L::NSLOT]);
-            }
-            __syncwarp();
-            return true;
-        };
-        auto issue_pv = [&](int t, int j) {
-            const int vu = 2 * j + 1;
-            if (!mbar_wait(p_full(t), j & 1)) return false;
-            if (!mbar_wait(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1)) return false;
-            tc::fence_after_sync();
-            const uint32_t dO = tmem + L::OCOL + t * D;
-            const uint32_t pcol = tmem + t * L::SCOL;
-            const uint64_t vd = kvdesc_v + (uint64_t)(((vu % L::NSLOT) * L::SLOT) >> 4);
-            if (lane == 0) {
+        for (int t = 0; t < L::QT; ++t) sq[t] = sp[t] = 0;
+        uint32_t idle = 0;
+        while (ok && (sp[0] < nt_t[0] || sp[1] < nt_t[1])) {
+            bool did = false;
 #pragma unroll
-                for (int kk = 0; kk < PN / 16; ++kk)
-                    tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
-                tc::commit(pv_done(t));
-                if (last_user(t, j)) tc::commit(&slot_empty[vu % L::NSLOT]);
-            }
-            __syncwarp();
-            return true;
-        };
-#pragma unroll 1
-        for (int t = 0; t < L::QT; ++t)
-            if (ok && nt_t[t] > 0) ok = issue_s(t, 0);
-        for (int j = 0; j < ntiles && ok; ++j) {
-#pragma unroll 1
             for (int t = 0; t < L::QT; ++t) {
-                if (!ok || j >= nt_t[t]) continue;
-                ok = issue_pv(t, j);
-                if (ok && j + 1 < nt_t[t]) ok = issue_s(t, j + 1);
+                const int o = t ^ 1;
+                const int u = sp[t];
+                if (u < sq[t]) {
+                    const int vu = 2 * u + 1;
+                    const bool rdy = mbar_test(p_full(t), u & 1) &&
+                                     mbar_test(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1);
+                    if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
+                        tc::fence_after_sync();
+                        const uint32_t dO = tmem + L::OCOL + t * D;
+                        const uint32_t pcol = tmem + t * L::SCOL;
+                        const uint64_t vd = kvdesc_v + (uint64_t)(((vu % L::NSLOT) * L::SLOT) >> 4);
+                        if (lane == 0) {
+#pragma unroll
+                            for (int kk = 0; kk < PN / 16; ++kk)
+                                tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
+                                                   (u > 0 || kk > 0) ? 1u : 0u);
+                            tc::commit(pv_done(t));
+                            if (sp[o] > u || u >= nt_t[o]) tc::commit(&slot_empty[vu % L::NSLOT]);
+                        }
+                        __syncwarp();
+                        sp[t] = u + 1;
+                        did = true;
+                    }
+                }
+                const int j = sq[t];
+                if (j < nt_t[t] && j == sp[t]) {
+                    const int ku = 2 * j;
+                    const bool rdy = mbar_test(&slot_full[ku % L::NSLOT], (ku / L::NSLOT) & 1);
+                    if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
+                        tc::fence_after_sync();
+                        const uint32_t dS = tmem + t * L::SCOL;
+                        const uint64_t qd = qdesc + (uint64_t)((t * L::QTILE) >> 4);
+                        const uint64_t kd = kvdesc_k + (uint64_t)(((ku % L::NSLOT) * L::SLOT) >> 4);
+                        if (lane == 0) {
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t qoff = (kk >> 2) * (PM * 128) + (kk & 3) * 32;
+                                const uint32_t koff = (kk >> 2) * L::HALF_OFF + (kk & 3) * 32;
+                                tc::mma_f16(dS, qd + (uint64_t)(qoff >> 4), kd + (uint64_t)(koff >> 4), idS,
+                                            kk > 0 ? 1u : 0u);
+                            }
+                            tc::commit(s_full(t));
+                            if (sq[o] > j || j >= nt_t[o]) tc::commit(&slot_empty[ku % L::NSLOT]);
+                        }
+                        __syncwarp();
+                        sq[t] = j + 1;
+                        did = true;
+                    }
+                }
+            }
+            if (did) {
+                idle = 0;
+            } else {
+                if (++idle > (1u << 24)) {
+                    if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+                    break;
+                }
+                if (idle > 8) __nanosleep(32);
             }
         }
-        if (!ok && lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
     } else {
         // ============================= softmax ======================================
-        // All eight warps work on one query tile at a time (tiles alternate A, B, A, ...),
-        // two warps per row: warp w owns rows 32 (w % 4) .. + 31 (its TMEM lanes) and
-        // the half h = w / 4 of the 128 keys of a K/V tile (and of O's columns).  The
-        // two halves of a row exchange their maxima through shared memory.
-        const int quad = warp & 3, half = warp >> 2;
-        const int r = quad * 32 + lane;                  // row within a query tile / TMEM lane
+        const int t = warp >> 2;                         // query tile of this warpgroup
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                  // row / TMEM lane
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        // the two warps of a row meet on an mbarrier (bounded waits), phase = meetings so far
-        uint64_t* pair = &pair_bars[quad];
-        int meets = 0;
-        auto meet = [&]() {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pair);
-            const bool met = mbar_wait(pair, meets & 1);
-            ++meets;
-            return met;
-        };
-        float* xmax = reinterpret_cast<float*>(smem + L::xmax);
-        float* xsum = reinterpret_cast<float*>(smem + L::xsum);
-        constexpr int DH = D / 2;                        // O columns per half
-        float m_ref[L::QT], l_run[L::QT];
-#pragma unroll
-        for (int t = 0; t < L::QT; ++t) {
-            m_ref[t] = -INFINITY;
-            l_run[t] = 0.f;
-        }
+        const uint32_t sbase = tmem + lane_addr + t * L::SCOL;
+        const uint32_t obase = tmem + lane_addr + L::OCOL + t * D;
+        const int R = t * PM + r;                        // row within the CTA
+        const int tok = R / G, g = R % G;
+        const int qi = i0 + tok;
+        const bool row_valid = qi < n;
+        const int last_key = c + qi;                     // row sees keys 0 .. last_key
+        const int first_key_t = c + i0 + t * L::TOKT;    // smallest last_key in this tile
+        const int nt = nt_t[t];
+        float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
-        int step = 0;                                    // (tile, query tile) steps done
-        for (int j = 0; j < ntiles && ok; ++j) {
+        for (int j = 0; j < nt && ok; ++j) {
+            const int k0 = j * PN;
+            if (!mbar_wait(s_full(t), j & 1)) {
+                report(p.dev_status, WF_DEV_TIMEOUT);
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            // keys some row of the tile may not see are masked.  The row max is taken on
+            // raw scores (scale > 0) and scaled once.  Two passes over S in 64-column
+            // halves: the maximum, then the weights.
+            const bool masked = (k0 + PN - 1 > first_key_t) || !row_valid;
+            float m8[8];
 #pragma unroll
-            for (int t = 0; t < L::QT; ++t) {
-                if (!ok || j >= nt_t[t]) continue;
-                const uint32_t sbase = tmem + lane_addr + t * L::SCOL;
-                const uint32_t obase = tmem + lane_addr + L::OCOL + t * D + half * DH;
-                const int R = t * PM + r;                // row within the CTA
-                const int qi = i0 + R / G;
-                const bool row_valid = qi < n;
-                const int last_key = c + qi;             // row sees keys 0 .. last_key
-                const int first_key_t = c + i0 + t * L::TOKT;   // smallest last_key in the tile
-                const int k0 = j * PN + half * 64;       // first key of this thread's half
-                if (!mbar_wait(s_full(t), j & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                float sa[32], sb[32];   // this thread's 64 scores: keys k0 .. k0 + 31, k0 + 32 .. k0 + 63
-                tc::ld_32cols(sbase + half * 64, sa);
-                tc::ld_32cols(sbase + half * 64 + 32, sb);
+            for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float s[2][32];
+                tc::ld_32cols(sbase + hh * 64, s[0]);
+                tc::ld_32cols(sbase + hh * 64 + 32, s[1]);
                 tc::wait_ld();
-                // keys some row of the tile may not see are masked; the row max is taken
-                // on raw scores (scale > 0) and scaled once
-                if ((j * PN + PN - 1 > first_key_t) || !row_valid) {
+                if (masked) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        sa[e] = (row_valid && k0 + e <= last_key) ? sa[e] : -INFINITY;
-                        sb[e] = (row_valid && k0 + 32 + e <= last_key) ? sb[e] : -INFINITY;
-                    }
+                    for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const bool vis = row_valid && k0 + hh * 64 + c2 * 32 + e <= last_key;
+                            s[c2][e] = vis ? s[c2][e] : -INFINITY;
+                        }
                 }
-                float m8[8];
+                // 8 independent running maxima (short dependency chains), two inputs a step
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmax3(sa[e], sa[e + 8], sb[e]);
+                for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmax3(m8[e], sa[e + 16], sa[e + 24]);
+                    for (int e = 0; e < 16; ++e) m8[e & 7] = fmax3(m8[e & 7], s[c2][e], s[c2][e + 16]);
+            }
+            const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const float mt = mraw * p.scale_log2;
+            // lazy online softmax: move the reference max only when it grows by > 2^8
+            float alpha = 1.f;
+            if (m_ref == -INFINITY) {
+                m_ref = mt;
+            } else if (mt > m_ref + kLazy) {
+                alpha = ex2(m_ref - mt);
+                m_ref = mt;
+            }
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                // O must hold P.V of tile j-1 before it is rescaled
+                if (!mbar_wait(pv_done(t), (j - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                tc::fence_after_sync();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmax3(m8[e], sb[e + 8], sb[e + 16]);
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    float o[32];
+                    tc::ld_32cols(obase + c4 * 32, o);
+                    tc::wait_ld();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], sb[e + 24]);
-                const float mhalf = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                          fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                // exchange with the other half of the row (buffers alternate by step, so a
-                // value is never overwritten before the partner has read it)
-                float* xm = xmax + (step & 1) * 2 * PM;
-                xm[half * PM + r] = mhalf;
-                if (!meet()) {
-                    ok = false;
-                    break;
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tc::st_32cols(obase + c4 * 32, o);
                 }
-                // every S column of these rows has now been read: P may overwrite them
-                const float mt = fmaxf(mhalf, xm[(half ^ 1) * PM + r]) * p.scale_log2;
-                ++step;
-                // lazy online softmax: move the reference max only when it grows by > 2^8
-                float alpha = 1.f;
-                if (m_ref[t] == -INFINITY) {
-                    m_ref[t] = mt;
-                } else if (mt > m_ref[t] + kLazy) {
-                    alpha = ex2(m_ref[t] - mt);
-                    m_ref[t] = mt;
-                }
-                l_run[t] *= alpha;
-                const float m_use = (m_ref[t] == -INFINITY) ? 0.f : m_ref[t];
-                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-                const float2 nm2 = make_float2(-m_use, -m_use);
-                float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                make_float2(0.f, 0.f)};
-                uint32_t pw[32];  // keys k0 + 2u, k0 + 2u + 1 as a bf16 pair
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
-                    const float2 x = __ffma2_rn(make_float2(sa[2 * u], sa[2 * u + 1]), sc2, nm2);
-                    const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
-                    ps[u & 3] = __fadd2_rn(ps[u & 3], e2);
-                    pw[u] = pack_bf16x2(e2.x, e2.y);
-                }
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float2 x = __ffma2_rn(make_float2(sb[2 * u], sb[2 * u + 1]), sc2, nm2);
-                    const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
-                    ps[u & 3] = __fadd2_rn(ps[u & 3], e2);
-                    pw[16 + u] = pack_bf16x2(e2.x, e2.y);
-                }
-                // P of keys [64 h, 64 h + 64) into columns [32 h, 32 h + 32)
-                tc::st_32words(sbase + half * 32, pw);
                 tc::wait_st();
-                // rescale this warp's half of O (rare); P.V of tile j waits for p_full below
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                    // O must hold P.V of tile j-1 before it is rescaled
-                    if (!mbar_wait(pv_done(t), (j - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
-                    tc::fence_after_sync();
+            }
+            l_run *= alpha;
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
 #pragma unroll 1
-                    for (int c4 = 0; c4 < DH / 32; ++c4) {
-                        float o[32];
-                        tc::ld_32cols(obase + c4 * 32, o);
-                        tc::wait_ld();
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pw[32];  // keys 2k, 2k+1 of this half as a bf16 pair
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tc::st_32cols(obase + c4 * 32, o);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    float s[32];
+                    tc::ld_32cols(sbase + hh * 64 + c2 * 32, s);
+                    tc::wait_ld();
+                    if (masked) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const bool vis = row_valid && k0 + hh * 64 + c2 * 32 + e <= last_key;
+                            s[e] = vis ? s[e] : -INFINITY;
+                        }
                     }
-                    tc::wait_st();
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
+                        const float2 x = __ffma2_rn(make_float2(s[2 * u], s[2 * u + 1]), sc2, nm2);
+                        const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
+                        ps[u & 3] = __fadd2_rn(ps[u & 3], e2);
+                        pw[c2 * 16 + u] = pack_bf16x2(e2.x, e2.y);
+                    }
                 }
-
-                const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
-                const float2 pst = __fadd2_rn(ps01, ps23);
-                l_run[t] += pst.x + pst.y;
-                if (j * PN + PN > kend) {
-                    // keys past the CTA's end were not loaded (or are stale): zero their V
-                    // rows once V_j has landed.  Warp half h zeroes the h-th 64-wide half
-                    // of key r's row.
-                    const int vu = 2 * j + 1;
-                    if (!mbar_wait(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1))
-                        report(p.dev_status, WF_DEV_TIMEOUT);
-                    if (half < L::NC && j * PN + r >= kend) {
+                // P of keys [64 hh, 64 hh + 64) into columns [32 hh, 32 hh + 32): S there
+                // has been read already
+                tc::st_32words(sbase + hh * 32, pw);
+            }
+            tc::wait_st();
+            const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
+            const float2 pst = __fadd2_rn(ps01, ps23);
+            l_run += pst.x + pst.y;
+            if (k0 + PN > kend) {
+                // keys past the CTA's end were not loaded (or are stale): zero their V
+                // rows once V_j has landed.  Thread r owns key r; when both groups take
+                // part in this last tile they write the same zeros.
+                const int vu = 2 * j + 1;
+                if (!mbar_wait(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
+                if (k0 + r >= kend) {
+#pragma unroll
+                    for (int cb = 0; cb < L::NC; ++cb) {
                         uint4* row = reinterpret_cast<uint4*>(unit_slot(vu) + (r >> 3) * L::ATOM +
-                                                              half * L::HALF_OFF + (r & 7) * 128);
+                                                              cb * L::HALF_OFF + (r & 7) * 128);
 #pragma unroll
                         for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
                     }
-                    tc::fence_proxy_async_smem();
                 }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full(t));
+                tc::fence_proxy_async_smem();
             }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(t));
         }
-        if (!ok) report(p.dev_status, WF_DEV_TIMEOUT);
-        // ---- epilogue: O / l -> bf16, each warp its half of O's columns --------------
-#pragma unroll
-        for (int t = 0; t < L::QT; ++t) xsum[(t * 2 + half) * PM + r] = l_run[t];
-        if (ok && !meet()) ok = false;
-#pragma unroll
-        for (int t = 0; t < L::QT; ++t) {
-            const int nt = nt_t[t];
-            if (!ok || nt == 0) continue;
-            const int R = t * PM + r;
-            const int qi = i0 + R / G, g = R % G;
-            const bool row_valid = qi < n;
-            const float l = l_run[t] + xsum[(t * 2 + (half ^ 1)) * PM + r];
+        // ---- epilogue: O / l -> bf16 --------------------------------------------------
+        if (ok && nt > 0) {
             if (!mbar_wait(pv_done(t), (nt - 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             tc::fence_after_sync();
-            const float inv = row_valid ? 1.f / l : 0.f;
-            const uint32_t obase = tmem + lane_addr + L::OCOL + t * D + half * DH;
+            const float inv = row_valid ? 1.f / l_run : 0.f;
 #pragma unroll
-            for (int c4 = 0; c4 < DH / 32; ++c4) {
+            for (int c4 = 0; c4 < D / 32; ++c4) {
                 float o[32];
                 tc::ld_32cols(obase + c4 * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
-                    __nv_bfloat16* dst =
-                        p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + half * DH + c4 * 32;
+                    __nv_bfloat16* dst = p.out + ((int64_t)(q_begin + qi) * p.H_q + h * G + g) * D + c4 * 32;
 #pragma unroll
                     for (int e8 = 0; e8 < 4; ++e8) {
                         uint4 v;
