@@ -408,7 +408,8 @@ def run_mixed(args, rank, world):
                    "D": g.D, "P": g.P},
         "roofline": {"kernel": "wf_paged_prefill", "bound": "tensor", "achieved": tflops, "peak": peak_t,
                      "unit": "TFLOP/s", "frac": tflops / peak_t, "peak_source": src,
-                     "algorithmic_flops_per_launch": flops, "avg_launch_us": pre_s * 1e6, "traffic": None},
+                     "algorithmic_flops_per_launch": flops, "avg_launch_us": pre_s * 1e6,
+                     "traffic": recorded_traffic("paged_prefill", "mixed_llama8b")},
         "decode_roofline": {"kernel": "wf_paged_decode", "bound": "hbm", "achieved": dbytes / dec_s / 1e9,
                             "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                             "frac": dbytes / dec_s / 1e9 / float(peaks["hbm_gbs"]),

@@ -69,26 +69,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return y;
 }
 
-// 2^x of two values on the FMA pipe, for x <= 8 (inputs below -125 give 2^-125):
-// Cody-Waite reduction x = n + f, n = round(x) (adding 1.5 * 2^23 rounds to an
-// integer held in the low mantissa bits), f in [-1/2, 1/2]; 2^f from a cubic whose
-// coefficients were fitted for least maximum relative error on [-1/2, 1/2] (7.5e-5);
-// 2^n is added to the exponent field.  Used beside ex2 to share the exponentials
-// between the FMA and MUFU pipes.
-__device__ __forceinline__ float2 exp2_fma2(float2 x) {
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 t = __fadd2_rn(x, make_float2(12582912.f, 12582912.f));
-    const float2 n = __fadd2_rn(t, make_float2(-12582912.f, -12582912.f));
-    const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
-    float2 p = __ffma2_rn(make_float2(0.055167440325021744f, 0.055167440325021744f), f,
-                          make_float2(0.24261078238487244f, 0.24261078238487244f));
-    p = __ffma2_rn(p, f, make_float2(0.6932617425918579f, 0.6932617425918579f));
-    p = __ffma2_rn(p, f, make_float2(0.9999281167984009f, 0.9999281167984009f));
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // Store n (1, 2 or 4) fp32 values as the storage type at p (naturally aligned).
 template <typename E, int n>
 __device__ __forceinline__ void store_out(void* p, const float* f);
