@@ -216,12 +216,16 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, 1) paged_decode_kernel(
     TileMeta* sMeta = reinterpret_cast<TileMeta*>(empty_bar + p.stages);
     float* sX = reinterpret_cast<float*>(sMeta + p.stages);   // [HC][parity][half][32][NF]
     float* sP = sX + p.HC * 2 * 2 * 32 * S::NF;                // [NCW][GMAX][T]
+    // [HC]: the two warps of a KV head meet here each tile (bounded waits, so a warp
+    // that stops on a timed-out wait cannot leave its partner blocked)
+    uint64_t* pair_bar = reinterpret_cast<uint64_t*>(sP + NCW * GMAX * T);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], NCW);
         }
+        for (int i = 0; i < p.HC; ++i) mbar_init(&pair_bar[i], 2);
         fence_mbar_init();
     }
     __syncthreads();
@@ -334,6 +338,7 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, 1) paged_decode_kernel(
     float2 acc[GMAX][S::VPL];
     float m_run = -INFINITY, l_run = 0.f;
     int hq0 = 0;
+    int meets = 0;
 
     for (int t = 0;; ++t) {
         const int st = t % p.stages;
@@ -419,7 +424,10 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, 1) paged_decode_kernel(
             const float* theirs = sXp + ((par * 2 + (1 - half)) * 32 + lane) * S::NF;
 #pragma unroll
             for (int j = 0; j < S::NF; ++j) mine[j] = v[j];
-            named_bar_sync(1 + pair, 64);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pair_bar[pair]);
+            if (!mbar_wait(&pair_bar[pair], meets & 1) && lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+            ++meets;
 #pragma unroll
             for (int j = 0; j < S::NF; ++j) v[j] += theirs[j];
         }
@@ -614,7 +622,7 @@ int smem_bytes_for(int hc, int stages) {
     using S = Shape<E, D, GMAX>;
     const int tile_bytes = S::T * hc * D * S::EB;
     return stages * (2 * tile_bytes + 16 + (int)sizeof(TileMeta)) + hc * 2 * 2 * 32 * S::NF * 4 +
-           2 * hc * GMAX * S::T * 4;
+           2 * hc * GMAX * S::T * 4 + hc * 8;
 }
 
 template <typename E, int D, int GMAX>

@@ -79,9 +79,9 @@ struct TcSmem {  // byte offsets from the 1024-aligned base
     static constexpr int qbuf = kStages * kStageBytes;
     static constexpr int pbuf = qbuf + 2 * kQBytes;
     static constexpr int bars = pbuf + 2 * kPBytes;
-    // full[3] empty[3] s_full[2] s_free[2] p_full[2] o_full[2] o_free[2] q_free[2]
-    static constexpr int nbars = 2 * kStages + 12;
-    static constexpr int meta = bars + nbars * 8;
+    // full[3] empty[3] s_full[2] s_free[2] p_full[2] o_full[2] o_free[2] q_free[2] grp
+    static constexpr int nbars = 2 * kStages + 13;
+    static constexpr int meta = (bars + nbars * 8 + 15) / 16 * 16;   // alpha/l/m below are read as float4
     static constexpr int alpha = meta + kStages * (int)sizeof(TcMeta);  // [2][kNq]
     static constexpr int lbuf = alpha + 2 * kNq * 4;                    // [2][kNq]
     static constexpr int mbuf = lbuf + 2 * kNq * 4;                     // [2][kNq]
@@ -89,6 +89,8 @@ struct TcSmem {  // byte offsets from the 1024-aligned base
     static constexpr int total = tmem_slot + 16;
 };
 static_assert(TcSmem::total + 1024 <= 232448, "tensor-core decode exceeds shared memory");
+static_assert(TcSmem::alpha % 16 == 0 && TcSmem::lbuf % 16 == 0 && TcSmem::mbuf % 16 == 0,
+              "alpha, l and m buffers are read with 16-byte loads");
 
 __device__ __forceinline__ unsigned char* stage_k(unsigned char* base, int st, int c) {
     return base + TcSmem::stage + st * kStageBytes + c * kHalf;
@@ -129,6 +131,9 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* o_full = p_full + 2;
     uint64_t* o_free = o_full + 2;
     uint64_t* q_free = o_free + 2;
+    // the four softmax warps meet here each tile (bounded waits, so a warp that stops
+    // on a timed-out wait cannot leave the others blocked)
+    uint64_t* grp = q_free + 2;
     TcMeta* meta = reinterpret_cast<TcMeta*>(smem + TcSmem::meta);
     float* alpha_buf = reinterpret_cast<float*>(smem + TcSmem::alpha);
     float* l_buf = reinterpret_cast<float*>(smem + TcSmem::lbuf);
@@ -158,6 +163,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&o_free[i], 4);
             mbar_init(&q_free[i], 1);
         }
+        mbar_init(grp, 4);
         fence_mbar_init();
     }
     // P^T is block-diagonal: zero both buffers once; only diagonal entries are rewritten.
@@ -451,7 +457,9 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
             tc::fence_proxy_async_smem();
-            named_bar_sync(1, 128);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(grp);
+            if (!mbar_wait(grp, t & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             if (lane == 0) mbar_arrive(&p_full[sb]);
             prev = m;
             have_prev = true;
