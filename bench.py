@@ -373,6 +373,61 @@ class MixedWorkload:
         return start.elapsed_time(end), pre, dec
 
 
+def run_cow(args, rank, world):
+    """Secondary line: the copy-on-write block copy of prefix sharing at Llama-3-8B
+    block size (32 KB a block and pool), 4096 pairs a call; 0.5 GB moved per call,
+    larger than L2."""
+    import torch
+    from paged_kv_cache_wf_gb300 import binding as wf
+    lib = wf.load()
+    geom, pairs = W.cow_copy_workload(n_pairs=4096, seed=rank)
+    shape = (geom.N, geom.P, geom.H_kv, geom.D)
+    gen = torch.Generator(device="cuda").manual_seed(11 + rank)
+    kp = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    vp = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    pr = torch.from_numpy(pairs).cuda()
+    desc = wf.pool_desc(kp)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = torch.cuda.current_stream().cuda_stream
+    block_bytes = geom.P * geom.H_kv * geom.D * 2
+    moved = 2 * 2 * pairs.shape[0] * block_bytes          # K and V, read and written
+
+    def call():
+        rc = lib.wf_copy_blocks(kp.data_ptr(), vp.data_ptr(), pr.data_ptr(), int(pairs.shape[0]), desc,
+                                status.data_ptr(), sp)
+        assert rc == 0, rc
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    if wf.wf_device_status_fetch(status) != 0:
+        raise SystemExit("device status flagged an error during warm-up")
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in evs:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    t = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    if rank == 0:
+        print(json.dumps({
+            "metric": "copy-on-write block copy (prefix sharing): blocks/s", "value": world * pairs.shape[0] / t,
+            "unit": "blocks/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "cow_copy_llama8b_block", "pairs": int(pairs.shape[0]), "block_bytes": block_bytes,
+                       "N": geom.N, "l2": "0.5 GB moved per call, larger than L2"},
+            "roofline": {"kernel": "wf_copy_blocks", "bound": "hbm", "achieved": moved / t / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": moved / t / 1e9 / hbm, "peak_source": src,
+                         "algorithmic_bytes_per_launch": moved, "avg_launch_us": t * 1e6, "traffic": None},
+            "gpu_launches": args.steps, "clocks": clk}), flush=True)
+
+
 def run_mixed(args, rank, world):
     """Secondary line: the mixed prefill + decode step (all three calls)."""
     import torch
@@ -521,7 +576,7 @@ def main():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--batch", type=int, default=231, choices=[118, 231])
-    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "gpt2", "llama1b", "mixed"])
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "gpt2", "llama1b", "mixed", "cow"])
     ap.add_argument("--impl", default="wf", choices=["wf", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -551,8 +606,8 @@ def main():
     if pg is not None:
         pg.barrier()
 
-    if args.workload == "mixed":
-        run_mixed(args, rank, world)
+    if args.workload in ("mixed", "cow"):
+        (run_mixed if args.workload == "mixed" else run_cow)(args, rank, world)
         if pg is not None:
             pg.destroy_process_group()
         return

@@ -88,6 +88,23 @@ wf_status wf_reshape_and_cache(const void* k, const void* v, void* k_pool, void*
                                wf_pool_desc pool, uint32_t* dev_status, cudaStream_t stream);
 
 /*
+ * wf_copy_blocks -- copy-on-write block copy for prefix sharing.
+ * (tiny-vllm-py, "Prefix Sharing": requests with a common prefix share its blocks,
+ *  and a shared, partly filled block is copied before a request appends to it;
+ *  ember, "Deliberately out of scope": copy-on-write block tables)
+ *
+ *   k_pool, v_pool  [N, P, H_kv, D], 16-byte aligned, modified in place
+ *   block_pairs     [num_pairs, 2] int32 device array of (src, dst) block ids:
+ *                   block dst of both pools becomes a byte copy of block src.
+ *   Destinations must be distinct and no block may be both a source and a
+ *   destination (the copies run in parallel); otherwise the result is undefined.
+ *   Ids outside [0, N) are skipped and flagged WF_DEV_BAD_BLOCK in *dev_status.
+ * num_pairs == 0 is a no-op.  Any pool dtype.
+ */
+wf_status wf_copy_blocks(void* k_pool, void* v_pool, const int32_t* block_pairs, int32_t num_pairs,
+                         wf_pool_desc pool, uint32_t* dev_status, cudaStream_t stream);
+
+/*
  * Bytes of caller-allocated device workspace wf_paged_decode needs for a batch
  * of at most B sequences of at most max_seq_len tokens.  Depends only on its
  * arguments; 0 if they are invalid.

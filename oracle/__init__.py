@@ -55,6 +55,8 @@ def _load():
             p, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
             lib.wfo_reshape_and_cache.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i32]
             lib.wfo_reshape_and_cache.restype = i32
+            lib.wfo_copy_blocks.argtypes = [p, p, p, i64, i64, i64, i64, i64, i32]
+            lib.wfo_copy_blocks.restype = i32
             lib.wfo_paged_decode.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, i64, i64, i64,
                                              d, i32, i32]
             lib.wfo_paged_decode.restype = i32
@@ -97,6 +99,17 @@ def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, dtype: str):
     T = int(slots.shape[0])
     _check(lib.wfo_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slots),
                                      T, N, P, H_kv, D, _DTYPES[dtype]), "wfo_reshape_and_cache")
+
+
+def copy_blocks(k_pool, v_pool, pairs, dtype: str):
+    """In-place copy-on-write block copy on numpy pools: block dst of both pools
+    becomes block src as it was before the call, for every (src, dst) row of pairs."""
+    lib = _load()
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    N, P, H_kv, D = k_pool.shape
+    pr = _c(np.asarray(pairs).reshape(-1, 2), np.int32)
+    _check(lib.wfo_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pr), int(pr.shape[0]), N, P, H_kv, D,
+                               _DTYPES[dtype]), "wfo_copy_blocks")
 
 
 def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, scale: float, dtype: str,

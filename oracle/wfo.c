@@ -57,6 +57,33 @@ int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_po
     return 0;
 }
 
+/* ---- block copy for copy-on-write (tiny-vllm-py "Prefix Sharing": a shared
+ * partial tail block is copied before a request appends to it) ------------ */
+int wfo_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int64_t n_pairs,
+                    int64_t N, int64_t P, int64_t H_kv, int64_t D, int dtype) {
+    if ((dtype != WFO_F32 && dtype != WFO_BF16) || n_pairs < 0 || N < 1 || P < 1 || H_kv < 1 || D < 1)
+        return WFO_ERR_ARG;
+    for (int64_t i = 0; i < 2 * n_pairs; ++i)
+        if (pairs[i] < 0 || pairs[i] >= N) return WFO_ERR_BLOCK;
+    if (n_pairs == 0) return 0;
+    const int64_t block_bytes = P * H_kv * D * elem_bytes(dtype);
+    /* every copy reads the pools as they were before the call */
+    char* snap = (char*)malloc((size_t)(2 * n_pairs * block_bytes));
+    if (!snap) return WFO_ERR_MEM;
+    for (int64_t i = 0; i < n_pairs; ++i) {
+        const int64_t src = pairs[2 * i];
+        memcpy(snap + (2 * i) * block_bytes, (const char*)k_pool + src * block_bytes, (size_t)block_bytes);
+        memcpy(snap + (2 * i + 1) * block_bytes, (const char*)v_pool + src * block_bytes, (size_t)block_bytes);
+    }
+    for (int64_t i = 0; i < n_pairs; ++i) {
+        const int64_t dst = pairs[2 * i + 1];
+        memcpy((char*)k_pool + dst * block_bytes, snap + (2 * i) * block_bytes, (size_t)block_bytes);
+        memcpy((char*)v_pool + dst * block_bytes, snap + (2 * i + 1) * block_bytes, (size_t)block_bytes);
+    }
+    free(snap);
+    return 0;
+}
+
 /* ---- one attention row: softmax over positions 0..len-1 of one sequence -- */
 typedef struct {
     const void* q;          /* query rows [rows, H_q, D]          */

@@ -45,6 +45,13 @@ int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_po
                           const int64_t* slot_mapping, int64_t T,
                           int64_t N, int64_t P, int64_t H_kv, int64_t D, int dtype);
 
+/* Copy-on-write block copy: for every pair i, block pairs[2i+1] of both pools
+ * becomes a byte copy of block pairs[2i] as it was before the call (a pair list
+ * with a repeated destination applies its pairs in order).  Any id outside
+ * [0, N) fails before anything is written. */
+int wfo_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int64_t n_pairs,
+                    int64_t N, int64_t P, int64_t H_kv, int64_t D, int dtype);
+
 /* Decode: out[b, g, :] = softmax_p(scale * q[b,g,:] . K_p) V_p over positions
  * p = 0 .. seq_lens[b]-1 of KV head g / (H_q/H_kv), gathered through
  * block_tables[b, :] (row-major [B, M]).  q is [B, H_q, D] in storage dtype. */

@@ -21,6 +21,7 @@ WF_DEV_BAD_SLOT, WF_DEV_BAD_BLOCK, WF_DEV_BAD_SEQLEN, WF_DEV_TIMEOUT = 0x1, 0x2,
 # every entry point include/wf.h declares
 EXPORTS = (
     "wf_reshape_and_cache",
+    "wf_copy_blocks",
     "wf_paged_decode_workspace_size",
     "wf_paged_decode",
     "wf_paged_prefill",
@@ -59,6 +60,8 @@ def load(path: str = LIB_PATH):
         vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
         lib.wf_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, wf_pool_desc, vp, vp]
         lib.wf_reshape_and_cache.restype = ctypes.c_int
+        lib.wf_copy_blocks.argtypes = [vp, vp, vp, i32, wf_pool_desc, vp, vp]
+        lib.wf_copy_blocks.restype = ctypes.c_int
         lib.wf_paged_decode_workspace_size.argtypes = [i32, i32, i32, wf_pool_desc]
         lib.wf_paged_decode_workspace_size.restype = sz
         lib.wf_paged_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, f32, wf_pool_desc,
@@ -139,6 +142,15 @@ def wf_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, dev_status=None, st
                                   int(slot_mapping.shape[0]), pool_desc(k_pool), _ptr(dev_status),
                                   _stream(stream))
     _check("wf_reshape_and_cache", rc)
+
+
+def wf_copy_blocks(k_pool, v_pool, block_pairs, dev_status=None, stream=None):
+    """Copy block src to block dst of both pools for every (src, dst) row of block_pairs [n, 2] int32."""
+    _contig(k_pool, v_pool, block_pairs)
+    lib = load()
+    rc = lib.wf_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(block_pairs), int(block_pairs.shape[0]),
+                            pool_desc(k_pool), _ptr(dev_status), _stream(stream))
+    _check("wf_copy_blocks", rc)
 
 
 def wf_paged_decode_workspace_size(B: int, num_q_heads: int, max_seq_len: int, desc: wf_pool_desc) -> int:

@@ -127,6 +127,18 @@ wf_status wf_reshape_and_cache(const void* k, const void* v, void* k_pool, void*
                                                   pool, dev_status, stream));
 }
 
+wf_status wf_copy_blocks(void* k_pool, void* v_pool, const int32_t* block_pairs, int32_t num_pairs,
+                         wf_pool_desc pool, uint32_t* dev_status, cudaStream_t stream) {
+    wf_status s = check_pool(pool);
+    if (s != WF_OK) return s;
+    if (num_pairs < 0) return WF_ERR_INVALID_ARG;
+    if (num_pairs == 0) return WF_OK;
+    if (!k_pool || !v_pool || !block_pairs) return WF_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(block_pairs) & 3u))
+        return WF_ERR_INVALID_ARG;
+    return from_cuda(wf::launch_copy_blocks(k_pool, v_pool, block_pairs, num_pairs, pool, dev_status, stream));
+}
+
 size_t wf_paged_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_seq_len,
                                       wf_pool_desc pool) {
     if (check_pool(pool) != WF_OK || num_q_heads < 1) return 0;

@@ -29,6 +29,8 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool,
                                      const int64_t* slot_mapping, int32_t num_tokens,
                                      const wf_pool_desc& pool, uint32_t* dev_status,
                                      cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int32_t num_pairs,
+                               const wf_pool_desc& pool, uint32_t* dev_status, cudaStream_t stream);
 
 // ---- decode -----------------------------------------------------------------
 // Positions are cut into fixed spans ("splits") that depend only on the pool

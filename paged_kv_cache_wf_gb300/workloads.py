@@ -456,6 +456,91 @@ WORKLOADS = {
 
 
 # ---------------------------------------------------------------------------
+# prefix sharing with copy-on-write (tiny-vllm-py, "Prefix Sharing"; ember's next
+# steps: "copy-on-write block tables")
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass
+class SharedPrefixStep:
+    """R requests share a cached prefix of c tokens, then each decodes one token.
+
+    Before the step every table points at the same prefix blocks (request 0 owns
+    them).  If c % P != 0 the last prefix block is partly filled and every other
+    request must write into it: it gets a private copy first (copy-on-write), and
+    its table is switched to the copy.  ``post`` is the step's decode layout (its
+    tables after the switch); ``cow_pairs`` the (source, destination) blocks to copy;
+    ``prefix_slots`` where the shared prefix was written (request 0's table).
+    """
+    geom: Geometry
+    prefix_len: int
+    pre_tables: np.ndarray     # int32 [R, M] before copy-on-write
+    post: Layout               # decode layout after it (seq_lens = c + 1)
+    cow_pairs: np.ndarray      # int32 [n, 2] (src, dst)
+    prefix_slots: np.ndarray   # int64 [c]
+
+
+def shared_prefix_step(H_q: int, H_kv: int, D: int, P: int, dtype: str, n_req: int, prefix_len: int,
+                       seed: int = 0, spare_blocks: int = 3) -> SharedPrefixStep:
+    rng = np.random.default_rng(seed)
+    c = int(prefix_len)
+    shared = _blocks_for(c, P)
+    partial = c % P != 0
+    # blocks: the shared prefix, plus per request either a copy of the partial tail
+    # (requests 1..R-1) or a fresh block for position c (when the prefix ends on a
+    # block boundary), plus spares
+    extra = (n_req - 1) if partial else n_req
+    N = shared + extra + spare_blocks
+    geom = Geometry(H_q=H_q, H_kv=H_kv, D=D, P=P, N=N, dtype=dtype)
+    alloc = BlockAllocator(N, rng)
+    prefix_blocks = [alloc.alloc() for _ in range(shared)]
+    pre_lists = [list(prefix_blocks) for _ in range(n_req)]
+    post_lists = [list(prefix_blocks) for _ in range(n_req)]
+    pairs = []
+    for r in range(n_req):
+        if partial:
+            if r > 0:
+                dst = alloc.alloc()
+                pairs.append((prefix_blocks[-1], dst))
+                post_lists[r][-1] = dst
+        else:
+            post_lists[r].append(alloc.alloc())
+    spare = alloc.alloc()
+    seq_lens = np.full(n_req, c + 1, dtype=np.int32)
+    post = Layout(geom, seq_lens, np.ones(n_req, np.int32), _tables_from_lists(post_lists, spare), spare)
+    pre_tables = _tables_from_lists(pre_lists, spare)
+    prefix_slots = (np.asarray(prefix_blocks, np.int64)[np.arange(c) // P] * P + np.arange(c) % P).astype(np.int64)
+    return SharedPrefixStep(geom, c, pre_tables, post, np.asarray(pairs, np.int32).reshape(-1, 2), prefix_slots)
+
+
+def draw_shared_prefix_values(step: SharedPrefixStep, rng) -> LayerValues:
+    """Values of a shared-prefix step: one prefix (repeated per request, so the
+    contiguous brute force sees every request's full sequence), one new token and
+    one query per request."""
+    g = step.geom
+    R, c, s = step.post.B, step.prefix_len, g.value_scale
+    kp = _draw(rng, (c, g.H_kv, g.D), g.dtype, s)
+    vp = _draw(rng, (c, g.H_kv, g.D), g.dtype, s)
+    return LayerValues(
+        q=_draw(rng, (R, g.H_q, g.D), g.dtype, s),
+        k_new=_draw(rng, (R, g.H_kv, g.D), g.dtype, s),
+        v_new=_draw(rng, (R, g.H_kv, g.D), g.dtype, s),
+        k_prefix=np.concatenate([kp] * R, axis=0) if R else kp[:0],
+        v_prefix=np.concatenate([vp] * R, axis=0) if R else vp[:0],
+    )
+
+
+def cow_copy_workload(H_kv: int = 8, D: int = 128, P: int = 16, n_pairs: int = 4096, seed: int = 0):
+    """Block pairs for timing the copy: n_pairs distinct sources and distinct
+    destinations drawn from a pool of 3 * n_pairs blocks (Llama-3-8B shapes: 32 KB a
+    block and pool)."""
+    rng = np.random.default_rng(seed)
+    N = 3 * n_pairs
+    perm = rng.permutation(N).astype(np.int32)
+    pairs = np.stack([perm[:n_pairs], perm[n_pairs:2 * n_pairs]], axis=1)
+    geom = Geometry(H_q=4 * H_kv, H_kv=H_kv, D=D, P=P, N=N, dtype=BF16)
+    return geom, pairs
+
+
+# ---------------------------------------------------------------------------
 # small custom layouts used by tests
 # ---------------------------------------------------------------------------
 def custom_layout(H_q: int, H_kv: int, D: int, P: int, dtype: str, seq_lens, q_lens=None,

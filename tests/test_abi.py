@@ -62,6 +62,18 @@ def test_scatter_argument_checks(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, _desc(P=0), None, None) == wf.WF_ERR_INVALID_ARG
 
 
+def test_copy_blocks_argument_checks(lib):
+    d = _desc()
+    f = lib.wf_copy_blocks
+    assert f(None, None, None, 0, d, None, None) == wf.WF_OK  # no pairs: no-op
+    assert f(None, None, None, 2, d, None, None) == wf.WF_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, -1, d, None, None) == wf.WF_ERR_INVALID_ARG
+    assert f(FAKE + 8, FAKE, FAKE, 2, d, None, None) == wf.WF_ERR_INVALID_ARG      # pool not 16-byte aligned
+    assert f(FAKE, FAKE, FAKE + 2, 2, d, None, None) == wf.WF_ERR_INVALID_ARG      # pairs not 4-byte aligned
+    assert f(FAKE, FAKE, FAKE, 2, _desc(D=96), None, None) == wf.WF_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 2, _desc(N=0), None, None) == wf.WF_ERR_INVALID_ARG
+
+
 def test_decode_workspace_size(lib):
     d = _desc(N=100, P=16, H=8, D=128)
     a = wf.wf_paged_decode_workspace_size(231, 32, 8704, d)

@@ -330,3 +330,61 @@ def test_oracle_thread_count_does_not_change_results():
     a = run_decode(lay, vals, 0.125, nthreads=1)
     b = run_decode(lay, vals, 0.125, nthreads=7)
     assert np.array_equal(a, b)
+
+
+# ---- copy-on-write block copy (tiny-vllm-py "Prefix Sharing") --------------------
+def _shared_prefix_pools(step, vals, cow=True):
+    """Oracle pools after the shared-prefix step: prefix written once through the
+    owner's table, tail blocks copied for the sharers, new tokens scattered."""
+    g = step.geom
+    kp, vp = W.empty_pool(g), W.empty_pool(g)
+    c = step.prefix_len
+    oracle.reshape_and_cache(vals.k_prefix[:c], vals.v_prefix[:c], kp, vp, step.prefix_slots, g.dtype)
+    if cow:
+        oracle.copy_blocks(kp, vp, step.cow_pairs, g.dtype)
+    oracle.reshape_and_cache(vals.k_new, vals.v_new, kp, vp, step.post.new_slots(), g.dtype)
+    return kp, vp
+
+
+@pytest.mark.parametrize("prefix_len,P,dtype", [(37, 16, W.F32), (32, 16, W.F32), (5, 4, W.BF16), (70, 7, W.BF16)])
+def test_prefix_sharing_with_copy_on_write_matches_brute_force(prefix_len, P, dtype):
+    """Requests share prefix blocks; sharers copy the partial tail before appending.
+    Decode through the pool equals the contiguous brute force (which never sees a
+    pool) for every request, and skipping the copy breaks it."""
+    step = W.shared_prefix_step(8, 2, 64, P, dtype, n_req=4, prefix_len=prefix_len, seed=prefix_len)
+    vals = W.draw_shared_prefix_values(step, np.random.default_rng(3))
+    scale = 1.0 / math.sqrt(64)
+    ref = brute_attention(step.post, vals, scale)
+    kp, vp = _shared_prefix_pools(step, vals)
+    got = oracle.paged_decode(vals.q, kp, vp, step.post.block_tables, step.post.seq_lens, scale, dtype)
+    assert np.max(np.abs(got - ref)) <= 1e-12
+    if step.cow_pairs.shape[0]:
+        kp2, vp2 = _shared_prefix_pools(step, vals, cow=False)
+        bad = oracle.paged_decode(vals.q, kp2, vp2, step.post.block_tables, step.post.seq_lens, scale, dtype)
+        assert not np.allclose(bad[1:], ref[1:], equal_nan=False)   # sharers read unwritten (NaN) rows
+        np.testing.assert_allclose(bad[0], ref[0], rtol=0, atol=1e-12)  # the owner kept the original
+
+
+def test_copy_blocks_leaves_sources_and_other_blocks_and_reads_before_writing():
+    """Sources and blocks no pair names keep their bytes; a block that is copied
+    and also copied from (src of one pair, dst of another) is read before it is
+    overwritten."""
+    g = W.Geometry(H_q=4, H_kv=2, D=64, P=4, N=6, dtype=W.BF16)
+    rng = np.random.default_rng(5)
+    kp = W._draw(rng, (g.N, g.P, g.H_kv, g.D), g.dtype, 1.0)
+    vp = W._draw(rng, (g.N, g.P, g.H_kv, g.D), g.dtype, 1.0)
+    k0, v0 = kp.copy(), vp.copy()
+    oracle.copy_blocks(kp, vp, np.array([[1, 4], [4, 2]], np.int32), g.dtype)   # 4 <- 1, 2 <- old 4
+    assert np.array_equal(kp[4], k0[1]) and np.array_equal(vp[4], v0[1])
+    assert np.array_equal(kp[2], k0[4]) and np.array_equal(vp[2], v0[4])
+    for blk in (0, 1, 3, 5):
+        assert np.array_equal(kp[blk], k0[blk]) and np.array_equal(vp[blk], v0[blk])
+
+
+def test_copy_blocks_rejects_out_of_range_ids_before_writing():
+    g = W.Geometry(H_q=4, H_kv=2, D=64, P=4, N=3, dtype=W.F32)
+    kp, vp = W.empty_pool(g), W.empty_pool(g)
+    k0 = kp.copy()
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(kp, vp, np.array([[0, 1], [0, 3]], np.int32), g.dtype)
+    assert np.array_equal(kp.view(np.uint32), k0.view(np.uint32))
