@@ -57,6 +57,16 @@ def _load():
             lib.wfo_reshape_and_cache.restype = i32
             lib.wfo_copy_blocks.argtypes = [p, p, p, i64, i64, i64, i64, i64, i32]
             lib.wfo_copy_blocks.restype = i32
+            f = ctypes.c_float
+            lib.wfo_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.wfo_e4m3_decode.restype = d
+            lib.wfo_e4m3_encode.argtypes = [f]
+            lib.wfo_e4m3_encode.restype = ctypes.c_uint8
+            lib.wfo_reshape_and_cache_fp8.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, f, f]
+            lib.wfo_reshape_and_cache_fp8.restype = i32
+            lib.wfo_paged_decode_fp8.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, i64, i64, i64,
+                                                 d, f, f, i32]
+            lib.wfo_paged_decode_fp8.restype = i32
             lib.wfo_paged_decode.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, i64, i64, i64,
                                              d, i32, i32]
             lib.wfo_paged_decode.restype = i32
@@ -110,6 +120,45 @@ def copy_blocks(k_pool, v_pool, pairs, dtype: str):
     pr = _c(np.asarray(pairs).reshape(-1, 2), np.int32)
     _check(lib.wfo_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pr), int(pr.shape[0]), N, P, H_kv, D,
                                _DTYPES[dtype]), "wfo_copy_blocks")
+
+
+def e4m3_decode(code: int) -> float:
+    return float(_load().wfo_e4m3_decode(int(code)))
+
+
+def e4m3_encode(y: float) -> int:
+    return int(_load().wfo_e4m3_encode(float(y)))
+
+
+def reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale: float, v_scale: float):
+    """In-place scatter of bf16 rows into uint8 (e4m3 code) pools [N, P, H_kv, D]."""
+    lib = _load()
+    assert k_pool.dtype == np.uint8 and k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    N, P, H_kv, D = k_pool.shape
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    _check(lib.wfo_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slots),
+                                         int(slots.shape[0]), N, P, H_kv, D, float(k_scale), float(v_scale)),
+           "wfo_reshape_and_cache_fp8")
+
+
+def paged_decode_fp8(q, k_pool, v_pool, block_tables, seq_lens, scale: float, k_scale: float, v_scale: float,
+                     nthreads: int | None = None) -> np.ndarray:
+    """fp64 decode outputs [B, H_q, D] for bf16 q and e4m3-code pools."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    k_pool = _c(k_pool, np.uint8)
+    v_pool = _c(v_pool, np.uint8)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    B, H_q, D = q.shape
+    N, P, H_kv, _ = k_pool.shape
+    out = np.zeros((B, H_q, D), np.float64)
+    _check(lib.wfo_paged_decode_fp8(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(bt), int(bt.shape[1]),
+                                    _ptr(sl), B, H_q, H_kv, D, N, P, float(scale), float(k_scale), float(v_scale),
+                                    nthreads or default_threads()), "wfo_paged_decode_fp8")
+    return out
 
 
 def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, scale: float, dtype: str,

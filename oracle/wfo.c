@@ -16,8 +16,44 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* ---- fp8 e4m3 (paged KV quantization, ember "Deliberately out of scope":
+ * "paged KV quantization (fp8/int8)") ---------------------------------------
+ * OCP FP8 E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent 0 is
+ * subnormal (2^-6 * m/8); S.1111.111 is NaN; no infinities; largest 448. */
+double wfo_e4m3_decode(uint8_t code) {
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Round to the nearest e4m3 value, ties to the even code; magnitudes above 448
+ * become 448 (saturating); NaN stays NaN; the sign of zero is kept.  Written as a
+ * search over the 127 finite magnitudes, plainly. */
+uint8_t wfo_e4m3_encode(float y) {
+    if (isnan(y)) return 0x7F;
+    const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    const double a = fabs((double)y);
+    if (a >= 448.0) return sign | 0x7E;
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double d = fabs(wfo_e4m3_decode((uint8_t)c) - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
 /* ---- exact widening of a stored element to double -------------------- */
 static double load_elem(const void* base, int64_t idx, int dtype) {
+    if (dtype == WFO_FP8) return wfo_e4m3_decode(((const uint8_t*)base)[idx]);
     if (dtype == WFO_F32) {
         float f;
         memcpy(&f, (const char*)base + idx * 4, 4);
@@ -33,7 +69,7 @@ static double load_elem(const void* base, int64_t idx, int dtype) {
     }
 }
 
-static int elem_bytes(int dtype) { return dtype == WFO_F32 ? 4 : 2; }
+static int elem_bytes(int dtype) { return dtype == WFO_F32 ? 4 : (dtype == WFO_FP8 ? 1 : 2); }
 
 /* ---- scatter (weft "Cache layouts": write = scatter via slot_mapping) -- */
 int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
@@ -53,6 +89,35 @@ int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_po
         const int64_t dst = (block * P + offset) * row_bytes;
         memcpy((char*)k_pool + dst, (const char*)k + t * row_bytes, (size_t)row_bytes);
         memcpy((char*)v_pool + dst, (const char*)v + t * row_bytes, (size_t)row_bytes);
+    }
+    return 0;
+}
+
+/* ---- scatter into an fp8 pool: code = e4m3(float(x) * (1 / scale)), with the
+ * reciprocal and the product rounded to float32 (the precision the device uses
+ * for this decision); k, v are bfloat16 [T, H_kv, D] ------------------------ */
+int wfo_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v_pool,
+                              const int64_t* slot_mapping, int64_t T, int64_t N, int64_t P,
+                              int64_t H_kv, int64_t D, float k_scale, float v_scale) {
+    if (T < 0 || N < 1 || P < 1 || H_kv < 1 || D < 1 || !(k_scale > 0.0f) || !(v_scale > 0.0f) ||
+        isinf(k_scale) || isinf(v_scale))
+        return WFO_ERR_ARG;
+    for (int64_t t = 0; t < T; ++t)
+        if (slot_mapping[t] >= N * P) return WFO_ERR_SLOT;
+    const float kinv = 1.0f / k_scale, vinv = 1.0f / v_scale;
+    const int64_t row = H_kv * D;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        const int64_t dst = ((slot / P) * P + slot % P) * row;
+        for (int64_t i = 0; i < row; ++i) {
+            const float xk = (float)load_elem(k, t * row + i, WFO_BF16);
+            const float xv = (float)load_elem(v, t * row + i, WFO_BF16);
+            volatile float yk = xk * kinv; /* one float32 rounding, no contraction */
+            volatile float yv = xv * vinv;
+            ((uint8_t*)k_pool)[dst + i] = wfo_e4m3_encode(yk);
+            ((uint8_t*)v_pool)[dst + i] = wfo_e4m3_encode(yv);
+        }
     }
     return 0;
 }
@@ -95,7 +160,9 @@ typedef struct {
     const int32_t* row_len;  /* query row -> number of positions   */
     int64_t rows, M, H_q, H_kv, D, N, P;
     double scale;
-    int dtype;
+    int dtype;              /* of q (and of the pools unless kv_dtype says fp8) */
+    int kv_dtype;
+    double k_scale, v_scale; /* dequantization: value = scale * stored value */
     double* out;
     int64_t next;            /* shared work counter (atomic)       */
     int status;
@@ -119,7 +186,7 @@ static int attend_row(const job_t* J, int64_t row, int64_t g, double* s, double*
         const int64_t kbase = ((block * J->P + offset) * J->H_kv + h) * J->D;
         double dot = 0.0;
         for (int64_t d = 0; d < J->D; ++d)
-            dot += load_elem(J->q, qbase + d, J->dtype) * load_elem(J->k_pool, kbase + d, J->dtype);
+            dot += load_elem(J->q, qbase + d, J->dtype) * (J->k_scale * load_elem(J->k_pool, kbase + d, J->kv_dtype));
         s[p] = J->scale * dot;
         if (s[p] > m) m = s[p];
     }
@@ -131,7 +198,8 @@ static int attend_row(const job_t* J, int64_t row, int64_t g, double* s, double*
         const int64_t offset = p % J->P;
         const int64_t vbase = ((block * J->P + offset) * J->H_kv + h) * J->D;
         den += w;
-        for (int64_t d = 0; d < J->D; ++d) acc[d] += w * load_elem(J->v_pool, vbase + d, J->dtype);
+        for (int64_t d = 0; d < J->D; ++d)
+            acc[d] += w * (J->v_scale * load_elem(J->v_pool, vbase + d, J->kv_dtype));
     }
     double* o = J->out + (row * J->H_q + g) * J->D;
     for (int64_t d = 0; d < J->D; ++d) o[d] = acc[d] / den;
@@ -195,11 +263,12 @@ static int check_common(const int32_t* block_tables, int64_t M, int64_t B, int64
 }
 
 /* ---- decode (one query per sequence; attends to all its positions) ---- */
-int wfo_paged_decode(double* out, const void* q, const void* k_pool, const void* v_pool,
-                     const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
-                     int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
-                     double scale, int dtype, int nthreads) {
-    int rc = check_common(block_tables, M, B, H_q, H_kv, D, N, P, dtype);
+static int decode_impl(double* out, const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
+                       int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
+                       double scale, int q_dtype, int kv_dtype, double k_scale, double v_scale,
+                       int nthreads) {
+    int rc = check_common(block_tables, M, B, H_q, H_kv, D, N, P, q_dtype);
     if (rc) return rc;
     for (int64_t b = 0; b < B; ++b)
         if (seq_lens[b] < 1 || seq_lens[b] > M * P) return WFO_ERR_LEN;
@@ -215,11 +284,28 @@ int wfo_paged_decode(double* out, const void* q, const void* k_pool, const void*
         row_len[b] = seq_lens[b];
     }
     job_t J = {q, k_pool, v_pool, block_tables, seq_lens, row_req, row_len,
-               B, M, H_q, H_kv, D, N, P, scale, dtype, out, 0, 0};
+               B, M, H_q, H_kv, D, N, P, scale, q_dtype, kv_dtype, k_scale, v_scale, out, 0, 0};
     rc = run_job(&J, nthreads);
     free(row_req);
     free(row_len);
     return rc;
+}
+
+int wfo_paged_decode(double* out, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
+                     int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
+                     double scale, int dtype, int nthreads) {
+    return decode_impl(out, q, k_pool, v_pool, block_tables, M, seq_lens, B, H_q, H_kv, D, N, P, scale,
+                       dtype, dtype, 1.0, 1.0, nthreads);
+}
+
+int wfo_paged_decode_fp8(double* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
+                         int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
+                         double scale, float k_scale, float v_scale, int nthreads) {
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || isinf(k_scale) || isinf(v_scale)) return WFO_ERR_ARG;
+    return decode_impl(out, q, k_pool, v_pool, block_tables, M, seq_lens, B, H_q, H_kv, D, N, P, scale,
+                       WFO_BF16, WFO_FP8, (double)k_scale, (double)v_scale, nthreads);
 }
 
 /* ---- prefill (causal varlen over the cached prefix plus the new rows) --- */
@@ -252,7 +338,7 @@ int wfo_paged_prefill(double* out, const void* q, const void* k_pool, const void
         }
     }
     job_t J = {q, k_pool, v_pool, block_tables, seq_lens, row_req, row_len,
-               rows, M, H_q, H_kv, D, N, P, scale, dtype, out, 0, 0};
+               rows, M, H_q, H_kv, D, N, P, scale, dtype, dtype, 1.0, 1.0, out, 0, 0};
     rc = run_job(&J, nthreads);
     free(row_req);
     free(row_len);

@@ -31,6 +31,7 @@ extern "C" {
 
 #define WFO_F32 0
 #define WFO_BF16 1
+#define WFO_FP8 2   /* e4m3 pool codes (queries and new rows stay bfloat16) */
 
 #define WFO_ERR_ARG   (-1)   /* shape / dtype argument invalid            */
 #define WFO_ERR_SLOT  (-2)   /* slot >= N*P                               */
@@ -44,6 +45,24 @@ extern "C" {
 int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                           const int64_t* slot_mapping, int64_t T,
                           int64_t N, int64_t P, int64_t H_kv, int64_t D, int dtype);
+
+/* fp8 e4m3 (OCP): the exact value of a code, and float -> code rounding to
+ * nearest (ties to the even code), saturating at +-448, NaN kept. */
+double wfo_e4m3_decode(uint8_t code);
+uint8_t wfo_e4m3_encode(float y);
+
+/* Scatter into fp8 pools: k, v are bfloat16 [T, H_kv, D]; each element is stored
+ * as e4m3(float(x) * (1.0f / scale)), the reciprocal and product rounded to float32.
+ * A stored code c stands for scale * value(c). */
+int wfo_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v_pool,
+                              const int64_t* slot_mapping, int64_t T, int64_t N, int64_t P,
+                              int64_t H_kv, int64_t D, float k_scale, float v_scale);
+
+/* Decode over fp8 pools (q bfloat16): K_p = k_scale * value(code), V_p likewise. */
+int wfo_paged_decode_fp8(double* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
+                         int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
+                         double scale, float k_scale, float v_scale, int nthreads);
 
 /* Copy-on-write block copy: for every pair i, block pairs[2i+1] of both pools
  * becomes a byte copy of block pairs[2i] as it was before the call (a pair list

@@ -388,3 +388,90 @@ def test_copy_blocks_rejects_out_of_range_ids_before_writing():
     with pytest.raises(oracle.OracleError):
         oracle.copy_blocks(kp, vp, np.array([[0, 1], [0, 3]], np.int32), g.dtype)
     assert np.array_equal(kp.view(np.uint32), k0.view(np.uint32))
+
+
+# ---- fp8 e4m3 KV pools (ember "Deliberately out of scope": paged KV quantization) ----
+def _torch():
+    return pytest.importorskip("torch")
+
+
+def test_e4m3_decode_matches_torch_float8_e4m3fn_for_all_codes():
+    torch = _torch()
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().double().numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_rounding_in_range_and_saturates_beyond():
+    torch = _torch()
+    rng = np.random.default_rng(7)
+    finite = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    mids = (finite[1:] + finite[:-1]) / 2                       # exact ties
+    ys = np.concatenate([rng.uniform(-464, 464, 4000), rng.standard_normal(2000) * 0.01, mids, -mids,
+                         finite, -finite, [0.0, -0.0, 2.0 ** -10, 2.0 ** -11]]).astype(np.float32)
+    ref = torch.from_numpy(ys).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(y)) for y in ys], np.uint8)
+    assert np.array_equal(got, ref)
+    for y, code in [(500.0, 0x7E), (-1e9, 0xFE), (float("inf"), 0x7E), (448.0, 0x7E)]:
+        assert oracle.e4m3_encode(y) == code
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def _fp8_case(seed=0, k_scale=0.0625, v_scale=0.25):
+    lay = W.custom_layout(8, 2, 64, 16, W.BF16, [40, 17, 64, 1], seed=seed)
+    vals = W.draw_layer_values(lay, np.random.default_rng(seed + 1))
+    g = lay.geom
+    shape = (g.N, g.P, g.H_kv, g.D)
+    kp, vp = np.full(shape, 0x7F, np.uint8), np.full(shape, 0x7F, np.uint8)   # NaN codes everywhere
+    oracle.reshape_and_cache_fp8(vals.k_prefix, vals.v_prefix, kp, vp, lay.prefix_slots(), k_scale, v_scale)
+    oracle.reshape_and_cache_fp8(vals.k_new, vals.v_new, kp, vp, lay.new_slots(), k_scale, v_scale)
+    return lay, vals, kp, vp
+
+
+def test_fp8_scatter_codes_match_torch_quantization():
+    """code = e4m3(float(x) * float32(1/scale)), checked against torch's float8 cast."""
+    torch = _torch()
+    k_scale, v_scale = 0.0625, 0.3
+    lay, vals, kp, vp = _fp8_case(k_scale=k_scale, v_scale=v_scale)
+    for rows, slots in ((vals.k_new, lay.new_slots()), (vals.k_prefix, lay.prefix_slots())):
+        x = torch.from_numpy(W.bf16_bits_to_f32(rows))
+        want = (x * torch.tensor(np.float32(1.0) / np.float32(k_scale))).to(torch.float8_e4m3fn).view(torch.uint8)
+        got = kp.reshape(-1, lay.geom.H_kv, lay.geom.D)[slots]
+        assert np.array_equal(got, want.numpy())
+    x = torch.from_numpy(W.bf16_bits_to_f32(vals.v_new))
+    want = (x * torch.tensor(np.float32(1.0) / np.float32(v_scale))).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(vp.reshape(-1, lay.geom.H_kv, lay.geom.D)[lay.new_slots()], want.numpy())
+
+
+def test_fp8_decode_matches_brute_force_on_dequantized_values():
+    """Decode over e4m3 pools equals the contiguous brute force on the dequantized
+    sequences (scale * value of each code, quantized here by torch), and swapping
+    the K and V scales breaks it."""
+    torch = _torch()
+    k_scale, v_scale = 0.0625, 0.25
+    lay, vals, kp, vp = _fp8_case(k_scale=k_scale, v_scale=v_scale)
+    g = lay.geom
+    scale = 1.0 / math.sqrt(g.D)
+    got = oracle.paged_decode_fp8(vals.q, kp, vp, lay.block_tables, lay.seq_lens, scale, k_scale, v_scale)
+
+    def deq(rows, s):
+        x = torch.from_numpy(W.bf16_bits_to_f32(rows))
+        c = (x * torch.tensor(np.float32(1.0) / np.float32(s))).to(torch.float8_e4m3fn)
+        return c.double().numpy() * s
+
+    q = W.storage_to_f64(vals.q, g.dtype)
+    cp, cq = lay.cu_prefix, lay.cu_q_lens
+    ref = np.zeros_like(got)
+    for b in range(lay.B):
+        K = np.concatenate([deq(vals.k_prefix[cp[b]:cp[b + 1]], k_scale), deq(vals.k_new[cq[b]:cq[b + 1]], k_scale)])
+        V = np.concatenate([deq(vals.v_prefix[cp[b]:cp[b + 1]], v_scale), deq(vals.v_new[cq[b]:cq[b + 1]], v_scale)])
+        for hq in range(g.H_q):
+            s = scale * (K[:, hq // g.G, :] @ q[b, hq])
+            w = np.exp(s - s.max())
+            ref[b, hq] = (w @ V[:, hq // g.G, :]) / w.sum()
+    assert np.max(np.abs(got - ref)) <= 1e-12
+    swapped = oracle.paged_decode_fp8(vals.q, kp, vp, lay.block_tables, lay.seq_lens, scale, v_scale, k_scale)
+    assert np.max(np.abs(swapped - ref)) > 1e-3
