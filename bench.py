@@ -139,17 +139,20 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # algorithmic bytes (what the method must move; no block padding)
 # ---------------------------------------------------------------------------
-def decode_bytes(lay) -> int:
+def decode_bytes(lay, kv_bytes=None) -> int:
     g = lay.geom
     e = W.elt_size(g.dtype)
-    kv = int(2 * lay.seq_lens.astype(np.int64).sum() * g.H_kv * g.D * e)
+    ekv = e if kv_bytes is None else kv_bytes
+    kv = int(2 * lay.seq_lens.astype(np.int64).sum() * g.H_kv * g.D * ekv)
     qo = 2 * lay.B * g.H_q * g.D * e
     tables = int(sum(-(-int(s) // g.P) for s in lay.seq_lens) * 4) + 4 * lay.B
     return kv + qo + tables
 
 
-def scatter_bytes(T: int, g) -> int:
-    return 2 * 2 * T * g.H_kv * g.D * W.elt_size(g.dtype) + 8 * T
+def scatter_bytes(T: int, g, kv_bytes=None) -> int:
+    e = W.elt_size(g.dtype)
+    ekv = e if kv_bytes is None else kv_bytes
+    return 2 * T * g.H_kv * g.D * (e + ekv) + 8 * T
 
 
 def prefill_flops(lay) -> float:
@@ -165,9 +168,13 @@ def prefill_flops(lay) -> float:
 # the wf arm
 # ---------------------------------------------------------------------------
 class DecodeWorkload:
-    """L layers of (scatter of B new tokens, paged decode), one pool per layer."""
+    """L layers of (scatter of B new tokens, paged decode), one pool per layer.
 
-    def __init__(self, lay, layers: int, seed: int):
+    kv="fp8": the pools hold e4m3 codes (one byte an element) of the same draws,
+    with k_scale = v_scale = value_scale / 64; q, the new rows and the outputs stay
+    bf16 and the scatter quantizes."""
+
+    def __init__(self, lay, layers: int, seed: int, kv: str = "bf16"):
         import torch
         from paged_kv_cache_wf_gb300 import binding as wf
         self.torch, self.wf = torch, wf
@@ -175,13 +182,19 @@ class DecodeWorkload:
         self.lay = lay
         g = lay.geom
         self.L = layers
-        self.pools = [W.device_pools(lay, seed=seed + 17 * l) for l in range(layers)]
+        self.kv = kv
+        self.k_scale = self.v_scale = 1.0
+        if kv == "fp8":
+            self.k_scale = self.v_scale = g.value_scale / 64.0
+            self.pools = [self._fp8_pools(seed + 17 * l) for l in range(layers)]
+        else:
+            self.pools = [W.device_pools(lay, seed=seed + 17 * l) for l in range(layers)]
         self.vals = [W.device_step_values(lay, seed=seed + 17 * l + 5) for l in range(layers)]
         self.outs = [torch.empty_like(v[0]) for v in self.vals]
         self.bt = torch.from_numpy(lay.block_tables).cuda()
         self.sl = torch.from_numpy(lay.seq_lens).cuda()
         self.slots = torch.from_numpy(lay.new_slots()).cuda()
-        self.desc = wf.pool_desc(self.pools[0][0])
+        self.desc = wf.pool_desc(self.pools[0][0], self.k_scale, self.v_scale)
         self.max_seq_len = lay.max_seq_len
         self.ws_bytes = wf.wf_paged_decode_workspace_size(lay.B, g.H_q, self.max_seq_len, self.desc)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
@@ -193,6 +206,19 @@ class DecodeWorkload:
 
     def split_span(self) -> int:
         return 128
+
+    def _fp8_pools(self, seed):
+        """e4m3 codes of the bf16 draws (torch's conversion after clamping to +-448;
+        NaN slots stay NaN codes)."""
+        torch = self.torch
+        kb, vb = W.device_pools(self.lay, seed=seed)
+        kp = (kb.float() / self.k_scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        vp = (vb.float() / self.v_scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        del kb, vb
+        return kp, vp
+
+    def kv_bytes(self) -> int:
+        return 1 if self.kv == "fp8" else W.elt_size(self.lay.geom.dtype)
 
     def _scatter(self, l, k=None, v=None, slots=None):
         kp, vp = self.pools[l]
@@ -479,7 +505,7 @@ def run_mixed(args, rank, world):
 # ---------------------------------------------------------------------------
 # the oracle (reference arm and CPU baseline)
 # ---------------------------------------------------------------------------
-def oracle_sample_inputs(lay, seed: int, wl=None):
+def oracle_sample_inputs(lay, seed: int, wl=None, kv: str = "bf16", kv_scales=(1.0, 1.0)):
     """Host inputs of one layer for the oracle: the blocks the batch uses and this
     step's new rows.  Taken from the device pools when a wf workload exists (the
     values the GPU sees), else drawn on the host."""
@@ -494,8 +520,10 @@ def oracle_sample_inputs(lay, seed: int, wl=None):
         remap[used] = np.arange(used.shape[0], dtype=np.int32)
         idx = torch.from_numpy(used.astype(np.int64)).cuda()
         bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+        codes = lambda t: t.cpu().numpy()
+        pool_host = codes if wl.kv == "fp8" else bits
         # pool contents before this step's write: the new slots are NaN in both
-        hk, hv = bits(kp.index_select(0, idx)), bits(vp.index_select(0, idx))
+        hk, hv = pool_host(kp.index_select(0, idx)), pool_host(vp.index_select(0, idx))
         bt = np.zeros_like(lay.block_tables)
         for b, n in enumerate(nb):
             bt[b, :n] = remap[lay.block_tables[b, :n]]
@@ -505,13 +533,19 @@ def oracle_sample_inputs(lay, seed: int, wl=None):
     rng = np.random.default_rng(seed)
     vals = W.draw_layer_values(lay, rng)
     import oracle
-    hk, hv = W.empty_pool(g), W.empty_pool(g)
-    oracle.reshape_and_cache(vals.k_prefix, vals.v_prefix, hk, hv, lay.prefix_slots(), g.dtype)
+    if kv == "fp8":
+        hk = np.full((g.N, g.P, g.H_kv, g.D), 0x7F, np.uint8)     # e4m3 NaN code
+        hv = hk.copy()
+        oracle.reshape_and_cache_fp8(vals.k_prefix, vals.v_prefix, hk, hv, lay.prefix_slots(), *kv_scales)
+    else:
+        hk, hv = W.empty_pool(g), W.empty_pool(g)
+        oracle.reshape_and_cache(vals.k_prefix, vals.v_prefix, hk, hv, lay.prefix_slots(), g.dtype)
     return lay, hk, hv, vals.q, vals.k_new, vals.v_new
 
 
-def oracle_time(sub, hk, hv, q, kn, vn, min_seconds: float, max_reps: int):
-    """Time scatter + decode of one layer of the batch in the oracle, repeated."""
+def oracle_time(sub, hk, hv, q, kn, vn, min_seconds: float, max_reps: int, fp8_scales=None):
+    """Time scatter + decode of one layer of the batch in the oracle, repeated
+    (fp8_scales = (k_scale, v_scale): e4m3 code pools)."""
     import oracle
     g = sub.geom
     scale = 1.0 / math.sqrt(g.D)
@@ -520,8 +554,13 @@ def oracle_time(sub, hk, hv, q, kn, vn, min_seconds: float, max_reps: int):
     reps, t0 = 0, time.perf_counter()
     while True:
         kp, vp = hk.copy(), hv.copy()
-        oracle.reshape_and_cache(kn, vn, kp, vp, slots, g.dtype)
-        oracle.paged_decode(q, kp, vp, sub.block_tables, sub.seq_lens, scale, g.dtype, threads)
+        if fp8_scales is not None:
+            ks, vs = fp8_scales
+            oracle.reshape_and_cache_fp8(kn, vn, kp, vp, slots, ks, vs)
+            oracle.paged_decode_fp8(q, kp, vp, sub.block_tables, sub.seq_lens, scale, ks, vs, threads)
+        else:
+            oracle.reshape_and_cache(kn, vn, kp, vp, slots, g.dtype)
+            oracle.paged_decode(q, kp, vp, sub.block_tables, sub.seq_lens, scale, g.dtype, threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or reps >= max_reps:
@@ -533,7 +572,8 @@ def oracle_time(sub, hk, hv, q, kn, vn, min_seconds: float, max_reps: int):
 # ---------------------------------------------------------------------------
 def make_layout(args):
     if args.workload == "llama8b":
-        return W.llama8b_decode(args.batch, seed=0), f"llama8b_decode_B{args.batch}"
+        sfx = "_fp8kv" if args.kv == "fp8" else ""
+        return W.llama8b_decode(args.batch, seed=0), f"llama8b_decode_B{args.batch}{sfx}"
     if args.workload == "gpt2":
         return W.gpt2_decode(0), "gpt2_decode_B32"
     if args.workload == "llama1b":
@@ -547,12 +587,13 @@ def run_reference(args, rank, world):
     lay, wname = make_layout(args)
     g = lay.geom
     L = g.L
-    sub, hk, hv, q, kn, vn = oracle_sample_inputs(lay, seed=0)
+    fp8 = (g.value_scale / 64.0,) * 2 if args.kv == "fp8" else None
+    sub, hk, hv, q, kn, vn = oracle_sample_inputs(lay, seed=0, kv=args.kv, kv_scales=fp8 or (1.0, 1.0))
     for _ in range(max(0, args.warmup)):
-        oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1)
+        oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1, fp8)
     times = []
     for _ in range(args.steps):
-        reps, el, threads = oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1)
+        reps, el, threads = oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1, fp8)
         times.append(el)
     per_layer = sum(times) / len(times)
     value = lay.B / per_layer
@@ -561,7 +602,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * L * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wname, "B": lay.B, "layers": L, "H_q": g.H_q, "H_kv": g.H_kv, "D": g.D,
-                   "P": g.P, "kv_dtype": g.dtype},
+                   "P": g.P, "kv_dtype": "fp8_e4m3" if fp8 else g.dtype},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"each timed step = one layer of the {wname} batch (all {lay.B} sequences, "
                                    f"scatter + decode) in the fp64 oracle; ms_per_step scales it to {L} layers"},
@@ -578,6 +619,8 @@ def main():
     ap.add_argument("--batch", type=int, default=231, choices=[118, 231])
     ap.add_argument("--workload", default="llama8b", choices=["llama8b", "gpt2", "llama1b", "mixed", "cow"])
     ap.add_argument("--impl", default="wf", choices=["wf", "reference"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="KV pool format of the decode workloads (fp8: e4m3 codes; Llama-3-8B shapes only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -611,10 +654,13 @@ def main():
         if pg is not None:
             pg.destroy_process_group()
         return
+    if args.kv == "fp8" and args.workload != "llama8b":
+        raise SystemExit("--kv fp8 runs the Llama-3-8B decode workload only")
     lay, wname = make_layout(args)
     g = lay.geom
     L = args.layers if args.layers > 0 else g.L
-    wl = DecodeWorkload(lay, L, seed=1000 + 7919 * rank)
+    wl = DecodeWorkload(lay, L, seed=1000 + 7919 * rank, kv=args.kv)
+    fp8 = (wl.k_scale, wl.v_scale) if args.kv == "fp8" else None
     # oracle inputs are copied before any kernel of ours has touched the pools
     oracle_in = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -643,12 +689,13 @@ def main():
 
     # ---- roofline of the decode call (split + combine kernels) -------------------
     peaks, peak_src = load_peaks()
-    dbytes = decode_bytes(lay)
+    kvb = wl.kv_bytes()
+    dbytes = decode_bytes(lay, kvb)
     avg_launch_s = (sum(launch_ms) / len(launch_ms)) / 1e3
     achieved = dbytes / avg_launch_s / 1e9
     hbm = float(peaks["hbm_gbs"])
-    step_bytes = L * (dbytes + scatter_bytes(lay.B, g))
-    traffic = recorded_traffic("paged_decode", wname)
+    step_bytes = L * (dbytes + scatter_bytes(lay.B, g, kvb))
+    traffic = recorded_traffic("paged_decode_fp8" if fp8 else "paged_decode", wname)
 
     # ---- end to end through host buffers --------------------------------------------
     e2e = None
@@ -672,8 +719,8 @@ def main():
     cpu = None
     if oracle_in is not None:
         sub, hk, hv, q, kn, vn = oracle_in
-        oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1)  # warm
-        reps, el, threads = oracle_time(sub, hk, hv, q, kn, vn, args.cpu_seconds, 1000)
+        oracle_time(sub, hk, hv, q, kn, vn, 0.0, 1, fp8)  # warm
+        reps, el, threads = oracle_time(sub, hk, hv, q, kn, vn, args.cpu_seconds, 1000, fp8)
         cpu = {"value": lay.B * reps / el, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"layer 0 of the {wname} batch (all {lay.B} sequences: scatter + decode), "
                          f"repeated {reps}x in {el:.1f} s with {threads} threads"}
@@ -682,12 +729,13 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "fp8e4m3 KV, f16 MMA" if fp8 else "bf16", "data": "synthetic",
             "config": {"workload": wname, "B": lay.B, "layers": L, "model_layers": g.L, "H_q": g.H_q,
-                       "H_kv": g.H_kv, "D": g.D, "P": g.P, "N_blocks_per_layer": g.N, "kv_dtype": g.dtype,
+                       "H_kv": g.H_kv, "D": g.D, "P": g.P, "N_blocks_per_layer": g.N,
+                       "kv_dtype": "fp8_e4m3" if fp8 else g.dtype,
                        "context_tokens": int(lay.seq_lens.sum()), "max_seq_len": lay.max_seq_len,
                        "l2": "inputs larger than L2: each layer's pools are %.2f GB, read once per step"
-                             % (2 * g.N * g.P * g.H_kv * g.D * 2 / 1e9),
+                             % (2 * g.N * g.P * g.H_kv * g.D * kvb / 1e9),
                        "parallelism": f"replicas{world}"},
             "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
             "pct_of_nominal_8tbs_step": 100.0 * step_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,

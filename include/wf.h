@@ -52,7 +52,15 @@ typedef enum wf_status {
     WF_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed                  */
 } wf_status;
 
-typedef enum wf_dtype { WF_DTYPE_F32 = 0, WF_DTYPE_BF16 = 1 } wf_dtype;
+typedef enum wf_dtype {
+    WF_DTYPE_F32 = 0,
+    WF_DTYPE_BF16 = 1,
+    /* fp8 e4m3 pools (OCP E4M3: 4 exponent bits, bias 7, 3 mantissa bits, largest
+     * 448, no infinities).  q, new k/v rows and outputs stay bfloat16; the pools
+     * hold codes that stand for k_scale * value (V: v_scale * value).
+     * (ember, "Deliberately out of scope": paged KV quantization (fp8/int8)) */
+    WF_DTYPE_FP8_E4M3 = 2
+} wf_dtype;
 
 /* Bits the kernels OR into *dev_status. */
 #define WF_DEV_BAD_SLOT    0x1u  /* slot_mapping[t] >= N*P: token t not written              */
@@ -67,7 +75,16 @@ typedef struct wf_pool_desc {
     int32_t block_size;    /* P: tokens per block, 1 .. 1024              */
     int32_t num_kv_heads;  /* H_kv                                        */
     int32_t head_dim;      /* D: 64 or 128                                */
-    int32_t dtype;         /* wf_dtype of q, k, v, pools and outputs      */
+    int32_t dtype;         /* wf_dtype of the pools; q, k, v and outputs
+                              have it too, except that fp8 pools take
+                              bfloat16 q, k, v and give bfloat16 outputs  */
+    float k_scale;         /* fp8 pools: a K code c stands for k_scale *
+                              value(c); the scatter stores
+                              e4m3(float(k) * (1.0f / k_scale)), rounded
+                              to nearest even and saturated at +-448.
+                              Must be finite and > 0 for fp8; ignored
+                              otherwise.                                  */
+    float v_scale;         /* the same for V                              */
 } wf_pool_desc;
 
 /*
@@ -133,6 +150,11 @@ size_t wf_paged_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t ma
  * Launches a split-K kernel and, when any sequence spans more than one split, a
  * combine kernel.  The split boundaries depend only on the pool geometry, so a
  * sequence's output does not depend on the rest of the batch.
+ * fp8 e4m3 pools: q and out are bfloat16; K_p and V_p are k_scale * value and
+ * v_scale * value of the stored codes.  Supported for H_kv = 8, D = 128, P a
+ * multiple of 16, H_q / H_kv in {2, 4} and N*P <= 2^31 - 1 (WF_ERR_UNSUPPORTED
+ * otherwise).  Both products run on the tensor cores in fp16 (every e4m3 value is
+ * an fp16 value, q is rounded to fp16, the softmax weights are rounded to fp16).
  */
 wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
                           const int32_t* block_tables, int32_t max_blocks_per_seq,

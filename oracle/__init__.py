@@ -28,8 +28,8 @@ _LIB_PATH = os.path.join(_HERE, "libwfo.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16 = 0, 1
-_DTYPES = {"f32": F32, "bf16": BF16}
+F32, BF16, FP8 = 0, 1, 2
+_DTYPES = {"f32": F32, "bf16": BF16, "fp8": FP8}   # fp8: e4m3 codes, uint8 pools
 
 
 def build(force: bool = False) -> str:

@@ -126,7 +126,8 @@ int wfo_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* 
  * partial tail block is copied before a request appends to it) ------------ */
 int wfo_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int64_t n_pairs,
                     int64_t N, int64_t P, int64_t H_kv, int64_t D, int dtype) {
-    if ((dtype != WFO_F32 && dtype != WFO_BF16) || n_pairs < 0 || N < 1 || P < 1 || H_kv < 1 || D < 1)
+    if ((dtype != WFO_F32 && dtype != WFO_BF16 && dtype != WFO_FP8) || n_pairs < 0 || N < 1 || P < 1 ||
+        H_kv < 1 || D < 1)
         return WFO_ERR_ARG;
     for (int64_t i = 0; i < 2 * n_pairs; ++i)
         if (pairs[i] < 0 || pairs[i] >= N) return WFO_ERR_BLOCK;

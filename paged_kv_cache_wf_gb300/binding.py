@@ -15,7 +15,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libwf.so")
 
 WF_OK, WF_ERR_INVALID_ARG, WF_ERR_UNSUPPORTED, WF_ERR_WORKSPACE, WF_ERR_CUDA = range(5)
-WF_DTYPE_F32, WF_DTYPE_BF16 = 0, 1
+WF_DTYPE_F32, WF_DTYPE_BF16, WF_DTYPE_FP8_E4M3 = 0, 1, 2
 WF_DEV_BAD_SLOT, WF_DEV_BAD_BLOCK, WF_DEV_BAD_SEQLEN, WF_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 # every entry point include/wf.h declares
@@ -35,7 +35,7 @@ EXPORTS = (
 class wf_pool_desc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class WfError(RuntimeError):
@@ -112,17 +112,20 @@ def _check(fn: str, rc: int):
         raise WfError(fn, rc)
 
 
-def pool_desc(k_pool) -> wf_pool_desc:
-    """Pool geometry from a [N, P, H_kv, D] float32 / bfloat16 tensor."""
+def pool_desc(k_pool, k_scale: float = 1.0, v_scale: float = 1.0) -> wf_pool_desc:
+    """Pool geometry from a [N, P, H_kv, D] float32 / bfloat16 tensor, or a uint8
+    tensor of fp8 e4m3 codes (with its dequantization scales)."""
     import torch
     N, P, H_kv, D = k_pool.shape
     if k_pool.dtype == torch.float32:
         dt = WF_DTYPE_F32
     elif k_pool.dtype == torch.bfloat16:
         dt = WF_DTYPE_BF16
+    elif k_pool.dtype == torch.uint8:
+        dt = WF_DTYPE_FP8_E4M3
     else:
         raise TypeError(f"unsupported pool dtype {k_pool.dtype}")
-    return wf_pool_desc(N, P, H_kv, D, dt)
+    return wf_pool_desc(N, P, H_kv, D, dt, float(k_scale), float(v_scale))
 
 
 def _contig(*ts):
@@ -134,22 +137,25 @@ def _contig(*ts):
 # ---------------------------------------------------------------------------
 # the C entry points, torch-tensor flavoured
 # ---------------------------------------------------------------------------
-def wf_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, dev_status=None, stream=None):
-    """Scatter k, v [T, H_kv, D] into k_pool, v_pool [N, P, H_kv, D] via slot_mapping [T] int64."""
+def wf_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, dev_status=None, stream=None,
+                         k_scale: float = 1.0, v_scale: float = 1.0):
+    """Scatter k, v [T, H_kv, D] into k_pool, v_pool [N, P, H_kv, D] via slot_mapping [T] int64
+    (uint8 pools: fp8 e4m3 codes of bf16 k, v quantized with k_scale, v_scale)."""
     _contig(k, v, k_pool, v_pool, slot_mapping)
     lib = load()
     rc = lib.wf_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping),
-                                  int(slot_mapping.shape[0]), pool_desc(k_pool), _ptr(dev_status),
-                                  _stream(stream))
+                                  int(slot_mapping.shape[0]), pool_desc(k_pool, k_scale, v_scale),
+                                  _ptr(dev_status), _stream(stream))
     _check("wf_reshape_and_cache", rc)
 
 
-def wf_copy_blocks(k_pool, v_pool, block_pairs, dev_status=None, stream=None):
+def wf_copy_blocks(k_pool, v_pool, block_pairs, dev_status=None, stream=None, k_scale: float = 1.0,
+                   v_scale: float = 1.0):
     """Copy block src to block dst of both pools for every (src, dst) row of block_pairs [n, 2] int32."""
     _contig(k_pool, v_pool, block_pairs)
     lib = load()
     rc = lib.wf_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(block_pairs), int(block_pairs.shape[0]),
-                            pool_desc(k_pool), _ptr(dev_status), _stream(stream))
+                            pool_desc(k_pool, k_scale, v_scale), _ptr(dev_status), _stream(stream))
     _check("wf_copy_blocks", rc)
 
 
@@ -158,14 +164,14 @@ def wf_paged_decode_workspace_size(B: int, num_q_heads: int, max_seq_len: int, d
 
 
 def wf_paged_decode(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len: int, scale: float,
-                    workspace, dev_status=None, stream=None):
+                    workspace, dev_status=None, stream=None, k_scale: float = 1.0, v_scale: float = 1.0):
     """out, q [B, H_q, D]; block_tables [B, M] int32; seq_lens [B] int32; workspace uint8 tensor."""
     _contig(out, q, k_pool, v_pool, block_tables, seq_lens)
     lib = load()
     B, H_q, _ = q.shape
     rc = lib.wf_paged_decode(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                              int(block_tables.shape[1]), _ptr(seq_lens), int(B), int(max_seq_len),
-                             int(H_q), float(scale), pool_desc(k_pool), _ptr(workspace),
+                             int(H_q), float(scale), pool_desc(k_pool, k_scale, v_scale), _ptr(workspace),
                              int(workspace.numel() * workspace.element_size()), _ptr(dev_status),
                              _stream(stream))
     _check("wf_paged_decode", rc)

@@ -30,12 +30,14 @@
 //            q buffers; mbarrier transaction counts mark arrival.
 //   warp 1   MMA issuer: S(t) into one of two TMEM S buffers, then O(t-1) = V^T P^T
 //            into one of two TMEM O buffers; commits free stages and buffers.
-//   warps 2-5  (thread i):  (a) as the owner of head dim d = i, accumulates the
-//            previous tile's O^T row into fp32 registers with the per-head rescale
-//            factors, and at the end of an item stores the output or the partial;
-//            (b) as the owner of row i = (head i/16, position i%16), runs the online
-//            softmax of the current tile for the head's G query heads (reductions
-//            over the 16 positions stay inside a half-warp) and writes P^T as bf16.
+//   warps 2-5  (thread i):  (a) as the owner of row i = (head i/16, position i%16),
+//            runs the online softmax of the current tile for the head's G query heads
+//            (reductions over the 16 positions stay inside a half-warp) and writes
+//            P^T as bf16; the four warps then meet and release P.V of the tile;
+//            (b) as the owner of head dim d = i, folds the previous tile's O^T row
+//            into fp32 registers with the per-head rescale factors, and at the end
+//            of an item stores the output or the partial.  Doing (b) after (a) keeps
+//            the wait for P.V(t-1) off the path from one softmax to the next.
 #include <cuda.h>
 
 #include "wf_internal.h"
@@ -66,6 +68,7 @@ struct TcParams {
     const int32_t* block_tables;
     const int32_t* seq_lens;
     uint32_t* dev_status;
+    uint32_t* queue;     // next unclaimed work item; zero at launch
     int32_t M, B, max_seq_len, H_q, H_kv, G, N, P, max_splits;
     float scale_log2;
 };
@@ -82,10 +85,10 @@ struct TcSmem {  // byte offsets from the 1024-aligned base
     // full[3] empty[3] s_full[2] s_free[2] p_full[2] o_full[2] o_free[2] q_free[2] grp
     static constexpr int nbars = 2 * kStages + 13;
     static constexpr int meta = (bars + nbars * 8 + 15) / 16 * 16;   // alpha/l/m below are read as float4
-    static constexpr int alpha = meta + kStages * (int)sizeof(TcMeta);  // [2][kNq]
-    static constexpr int lbuf = alpha + 2 * kNq * 4;                    // [2][kNq]
-    static constexpr int mbuf = lbuf + 2 * kNq * 4;                     // [2][kNq]
-    static constexpr int tmem_slot = mbuf + 2 * kNq * 4;
+    static constexpr int alpha = meta + kStages * (int)sizeof(TcMeta);  // [3][kNq]: tile t in t % 3
+    static constexpr int lbuf = alpha + 3 * kNq * 4;                    // [3][kNq]: item k in k % 3
+    static constexpr int mbuf = lbuf + 3 * kNq * 4;                     // [3][kNq]
+    static constexpr int tmem_slot = mbuf + 3 * kNq * 4;
     static constexpr int total = tmem_slot + 16;
 };
 static_assert(TcSmem::total + 1024 <= 232448, "tensor-core decode exceeds shared memory");
@@ -183,7 +186,12 @@ __global__ void __launch_bounds__(192, 1)
         int b = 0, len = 0, nsp = -1;
         int64_t cum = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; ok; item += gridDim.x) {
+        // Items come from a queue shared by all CTAs (one atomic increment per item,
+        // claimed one item ahead so the round trip overlaps the current item's
+        // copies).  Each CTA's claims increase, so the walk over sequences below
+        // only moves forward.
+        uint32_t claim = lane == 0 ? atomicAdd(p.queue, 1u) : 0u;
+        for (int64_t item = __shfl_sync(0xffffffffu, claim, 0); ok; item = __shfl_sync(0xffffffffu, claim, 0)) {
             while (b < p.B) {
                 if (nsp < 0) {
                     len = __ldg(p.seq_lens + b);
@@ -200,6 +208,7 @@ __global__ void __launch_bounds__(192, 1)
                 nsp = -1;
             }
             if (b >= p.B) break;
+            claim = lane == 0 ? atomicAdd(p.queue, 1u) : 0u;
             const int split = (int)(item - cum);
             const int s0 = split * kSpanTc;
             const int s1 = min(len, s0 + kSpanTc);
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(192, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_free[ub]);
-            const float* al = alpha_buf + ub * kNq;
+            const float* al = alpha_buf + (u % 3) * kNq;
 #pragma unroll
             for (int c = 0; c < HQ; c += 4) {
                 const float4 a4 = ld_shared_f4(al + c);
@@ -365,8 +374,8 @@ __global__ void __launch_bounds__(192, 1)
                 acc[c + 3] = acc[c + 3] * a4.w + o[c + 3];
             }
             if (m.last) {
-                const float* L = l_buf + (m.item & 1) * kNq;
-                const float* Mx = m_buf + (m.item & 1) * kNq;
+                const float* L = l_buf + (m.item % 3) * kNq;
+                const float* Mx = m_buf + (m.item % 3) * kNq;
                 if (m.nsplit == 1) {
                     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (int64_t)m.b * p.H_q * kD + i;
 #pragma unroll
@@ -389,10 +398,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             const TcMeta m = meta[st];
             if (m.nvalid == kEndTile) break;
-            // (a) fold in the previous tile's P.V (reads alpha written before the last barrier)
-            if (have_prev) accumulate(t - 1, prev);
-
-            // (b) softmax of this tile
+            // (a) softmax of this tile
             const int sb = t & 1;
             if (!mbar_wait(&s_full[sb], (t >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             tc::fence_after_sync();
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (pos == 0) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) alpha_buf[sb * kNq + hk * G + g] = al[g];
+                for (int g = 0; g < G; ++g) alpha_buf[(t % 3) * kNq + hk * G + g] = al[g];
             }
             if (m.last) {
 #pragma unroll
@@ -442,8 +448,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int mask = 8; mask >= 1; mask >>= 1) x += __shfl_xor_sync(0xffffffffu, x, mask);
                     if (pos == 0) {
-                        l_buf[(m.item & 1) * kNq + hk * G + g] = x;
-                        m_buf[(m.item & 1) * kNq + hk * G + g] = m_run[g];
+                        l_buf[(m.item % 3) * kNq + hk * G + g] = x;
+                        m_buf[(m.item % 3) * kNq + hk * G + g] = m_run[g];
                     }
                 }
             }
@@ -461,6 +467,10 @@ __global__ void __launch_bounds__(192, 1)
             if (lane == 0) mbar_arrive(grp);
             if (!mbar_wait(grp, t & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             if (lane == 0) mbar_arrive(&p_full[sb]);
+            // (b) fold in the previous tile's P.V while this tile's runs: it completed
+            // during this softmax (alpha of tile t-1 sits in ring slot (t-1) % 3, which
+            // softmax(t+2) rewrites only after every warp has met at tile t+1)
+            if (have_prev) accumulate(t - 1, prev);
             prev = m;
             have_prev = true;
         }
@@ -490,7 +500,7 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
                                    const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                                    int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
-                                   float2* ws_ml, int32_t max_splits, uint32_t* dev_status,
+                                   float2* ws_ml, int32_t max_splits, uint32_t* queue, uint32_t* dev_status,
                                    cudaStream_t stream) {
     const int G = num_q_heads / pool.num_kv_heads;
     CUtensorMap tm_k, tm_v, tm_q;
@@ -519,6 +529,7 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.dev_status = dev_status;
+    p.queue = queue;
     p.M = max_blocks_per_seq;
     p.B = B;
     p.max_seq_len = max_seq_len;

@@ -45,6 +45,11 @@ cudaError_t allow_dynamic_smem(const void* kernel, int bytes) {
 
 cudaError_t encode_tiled_bf16(CUtensorMap* map, void* base, int rank, const uint64_t* dims,
                               const uint64_t* strides, const uint32_t* box) {
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box);
+}
+
+cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box) {
     static std::mutex mu;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     {
@@ -66,7 +71,7 @@ cudaError_t encode_tiled_bf16(CUtensorMap* map, void* base, int rank, const uint
         es[i] = 1;
         if (i + 1 < rank) s[i] = strides[i];
     }
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, base, d, s, bx, es,
+    const CUresult r = fn(map, type, (cuuint32_t)rank, base, d, s, bx, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -82,7 +87,11 @@ wf_status check_pool(const wf_pool_desc& pool) {
     if (pool.num_blocks < 1 || pool.block_size < 1 || pool.block_size > 1024 ||
         pool.num_kv_heads < 1)
         return WF_ERR_INVALID_ARG;
-    if (pool.dtype != WF_DTYPE_F32 && pool.dtype != WF_DTYPE_BF16) return WF_ERR_UNSUPPORTED;
+    if (pool.dtype != WF_DTYPE_F32 && pool.dtype != WF_DTYPE_BF16 && pool.dtype != WF_DTYPE_FP8_E4M3)
+        return WF_ERR_UNSUPPORTED;
+    if (pool.dtype == WF_DTYPE_FP8_E4M3 &&
+        !(pool.k_scale > 0.f && pool.v_scale > 0.f && pool.k_scale <= 3.0e38f && pool.v_scale <= 3.0e38f))
+        return WF_ERR_INVALID_ARG;
     if (pool.head_dim != 64 && pool.head_dim != 128) return WF_ERR_UNSUPPORTED;
     const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
     if (slots > (int64_t)INT32_MAX * 64) return WF_ERR_INVALID_ARG;
@@ -99,7 +108,7 @@ wf_status from_cuda(cudaError_t e) {
 
 extern "C" {
 
-int wf_abi_version(void) { return 100; }
+int wf_abi_version(void) { return 101; }
 
 const char* wf_status_string(wf_status s) {
     switch (s) {
@@ -156,6 +165,10 @@ wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const vo
     if (B < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 1) return WF_ERR_INVALID_ARG;
     if (num_q_heads % pool.num_kv_heads != 0) return WF_ERR_INVALID_ARG;
     if (num_q_heads / pool.num_kv_heads > 8) return WF_ERR_UNSUPPORTED;
+    if (pool.dtype == WF_DTYPE_FP8_E4M3 &&
+        (!wf::decode_tc_fp8_supported(pool, num_q_heads) ||
+         (int64_t)pool.num_blocks * pool.block_size > INT32_MAX))
+        return WF_ERR_UNSUPPORTED;
     if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool.block_size) return WF_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return WF_ERR_INVALID_ARG;
     if (B == 0) return WF_OK;

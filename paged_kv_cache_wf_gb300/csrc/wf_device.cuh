@@ -6,6 +6,8 @@
 #include <cstdint>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "../../include/wf.h"
@@ -60,6 +62,34 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 16 bfloat16 values (two 16-byte chunks) -> 16 fp8 e4m3 codes: x * inv rounded to
+// float32, then to e4m3 with round-to-nearest-even and saturation (NaN kept).
+__device__ __forceinline__ void quantize16_e4m3(const uint4& lo, const uint4& hi, float inv, uint4& out) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = bf16x2_to_float2(w[2 * i]), b = bf16x2_to_float2(w[2 * i + 1]);
+        const uint32_t c0 = __nv_cvt_float2_to_fp8x2(make_float2(a.x * inv, a.y * inv), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(b.x * inv, b.y * inv), __NV_SATFINITE, __NV_E4M3);
+        o[i] = (c0 & 0xffffu) | (c1 << 16);
+    }
+    out = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 16 fp8 e4m3 codes (one 16-byte chunk) -> 16 fp16 values, exactly, as 8 words
+// (element 2i in the low half of word i).
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4& c, uint32_t (&w)[8]) {
+    const uint32_t in[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(in[i] & 0xffffu), __NV_E4M3);
+        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(in[i] >> 16), __NV_E4M3);
+        w[2 * i] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+        w[2 * i + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+    }
 }
 
 // max(a, b, c) in one instruction.
@@ -282,6 +312,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
     return (1u << 4)                       // D format: f32
            | (1u << 7)                     // A format: bf16
            | (1u << 10)                    // B format: bf16
+           | ((uint32_t)a_mn_major << 15)  // A major-ness
+           | ((uint32_t)b_mn_major << 16)  // B major-ness
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor, kind::f16 with fp16 A and B, fp32 D, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4)                       // D format: f32 (A, B format 0: f16)
            | ((uint32_t)a_mn_major << 15)  // A major-ness
            | ((uint32_t)b_mn_major << 16)  // B major-ness
            | ((uint32_t)(N >> 3) << 17)    // N / 8

@@ -12,7 +12,7 @@
 
 namespace wf {
 
-inline int dtype_bytes(int32_t dtype) { return dtype == WF_DTYPE_F32 ? 4 : 2; }
+inline int dtype_bytes(int32_t dtype) { return dtype == WF_DTYPE_F32 ? 4 : (dtype == WF_DTYPE_FP8_E4M3 ? 1 : 2); }
 
 // SM count of the current device (cached per device).
 int num_sms();
@@ -24,6 +24,8 @@ cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
 // dims[0] is the contiguous dimension; strides[] are bytes for dims 1..rank-1.
 cudaError_t encode_tiled_bf16(CUtensorMap* map, void* base, int rank, const uint64_t* dims,
                               const uint64_t* strides, const uint32_t* box);
+cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box);
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                      const int64_t* slot_mapping, int32_t num_tokens,
@@ -63,8 +65,18 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
                                    const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                                    int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
-                                   float2* ws_ml, int32_t max_splits, uint32_t* dev_status,
+                                   float2* ws_ml, int32_t max_splits, uint32_t* queue, uint32_t* dev_status,
                                    cudaStream_t stream);
+
+// Tensor-core decode over fp8 e4m3 pools (H_kv = 8, D = 128, P % 16 == 0,
+// G in {2, 4}; bf16 q and outputs); same partials as the bf16 kernel.
+bool decode_tc_fp8_supported(const wf_pool_desc& pool, int32_t num_q_heads);
+cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                                       int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
+                                       float2* ws_ml, int32_t max_splits, uint32_t* queue,
+                                       uint32_t* dev_status, cudaStream_t stream);
 
 // ---- prefill ------------------------------------------------------------------
 // Pipelined tcgen05 prefill (bf16, P % 16 == 0, G in {1, 2, 4, 8}, D in {64, 128}).

@@ -41,13 +41,17 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.wf_abi_version() == 100
+    assert lib.wf_abi_version() == 101
     for code in range(5):
         assert wf.status_string(code)
 
 
-def _desc(N=10, P=16, H=2, D=64, dt=wf.WF_DTYPE_BF16):
-    return wf.wf_pool_desc(N, P, H, D, dt)
+def _desc(N=10, P=16, H=2, D=64, dt=wf.WF_DTYPE_BF16, ks=0.0, vs=0.0):
+    return wf.wf_pool_desc(N, P, H, D, dt, ks, vs)
+
+
+def _fp8(N=10, P=16, H=8, D=128, ks=0.05, vs=0.05):
+    return _desc(N, P, H, D, wf.WF_DTYPE_FP8_E4M3, ks, vs)
 
 
 def test_scatter_argument_checks(lib):
@@ -141,3 +145,33 @@ def _load_fresh(path):
         return wf.load(path)
     finally:
         wf._lib = saved
+
+
+def test_fp8_pool_argument_checks(lib):
+    """fp8 e4m3 pools need finite positive scales; decode takes them only in the
+    shapes the tensor-core kernel handles; prefill does not take them."""
+    sc = lib.wf_reshape_and_cache
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        assert sc(FAKE, FAKE, FAKE, FAKE, FAKE, 0, _fp8(ks=ks, vs=vs), None, None) == wf.WF_ERR_INVALID_ARG
+    assert sc(None, None, None, None, None, 0, _fp8(), None, None) == wf.WF_OK
+    assert lib.wf_copy_blocks(FAKE, FAKE, FAKE, 0, _fp8(), None, None) == wf.WF_OK
+    assert lib.wf_copy_blocks(FAKE, FAKE, FAKE, 0, _fp8(ks=0.0), None, None) == wf.WF_ERR_INVALID_ARG
+
+    f = lib.wf_paged_decode
+
+    def dec(d, Hq=32, B=0):
+        ws = wf.wf_paged_decode_workspace_size(4, Hq, 64, d)
+        return f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, B, 64, Hq, 0.1, d, FAKE, ws, None, None)
+
+    assert dec(_fp8()) == wf.WF_OK                                    # G = 4: supported (B = 0: no-op)
+    assert dec(_fp8(), Hq=16) == wf.WF_OK                             # G = 2
+    assert dec(_fp8(), Hq=8) == wf.WF_ERR_UNSUPPORTED                 # G = 1
+    assert dec(_fp8(), Hq=64) == wf.WF_ERR_UNSUPPORTED                # G = 8
+    assert dec(_fp8(D=64)) == wf.WF_ERR_UNSUPPORTED
+    assert dec(_fp8(H=4), Hq=16) == wf.WF_ERR_UNSUPPORTED
+    assert dec(_fp8(P=8)) == wf.WF_ERR_UNSUPPORTED
+    assert dec(_fp8(ks=0.0)) == wf.WF_ERR_INVALID_ARG
+
+    pf = lib.wf_paged_prefill
+    rc = pf(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 8, 8, 64, 32, 0.1, _fp8(), None, None)
+    assert rc == wf.WF_ERR_UNSUPPORTED

@@ -182,3 +182,27 @@ def test_decode_empty_batch_is_a_no_op():
     sl = torch.zeros(0, dtype=torch.int32, device="cuda")
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     wf.wf_paged_decode(out, q, kp, kp.clone(), bt, sl, 16, 0.125, ws)
+
+
+@pytest.mark.parametrize("H_q,H_kv,D,P", [(32, 8, 128, 16), (8, 2, 64, 16)])
+def test_decode_workspace_left_dirty_is_fine_and_reusable(H_q, H_kv, D, P):
+    """The workspace needs no initialisation: filled with 0xFF bytes, then reused by
+    a second call, it gives the same bytes both times, within tolerance of the oracle
+    (the tensor-core kernels keep their work-item queue in it)."""
+    torch = G.torch_mod()
+    lay = W.custom_layout(H_q, H_kv, D, P, W.BF16, [3000, 5, 129, 640, 1, 2048], seed=12)
+    vals = W.draw_layer_values(lay, np.random.default_rng(12))
+    kp, vp = G.build_dev_pools(lay, vals)
+    q = G.to_dev(vals.q, W.BF16)
+    ws = torch.full((wf.wf_paged_decode_workspace_size(lay.B, H_q, lay.max_seq_len, wf.pool_desc(kp)),), 255,
+                    dtype=torch.uint8, device="cuda")
+    bt, sl = torch.from_numpy(lay.block_tables).cuda(), torch.from_numpy(lay.seq_lens).cuda()
+    outs = []
+    for _ in range(2):
+        out = torch.empty_like(q)
+        st = G.dev_status()
+        wf.wf_paged_decode(out, q, kp, vp, bt, sl, lay.max_seq_len, 0.088, ws, st)
+        assert wf.wf_device_status_fetch(st) == 0
+        outs.append(G.storage_bytes(out))
+    assert np.array_equal(outs[0], outs[1])
+    G.assert_close(G.from_dev(out, W.BF16), _oracle_decode(lay, vals, 0.088), W.BF16, "dirty workspace")

@@ -381,6 +381,19 @@ def test_copy_blocks_leaves_sources_and_other_blocks_and_reads_before_writing():
         assert np.array_equal(kp[blk], k0[blk]) and np.array_equal(vp[blk], v0[blk])
 
 
+def test_copy_blocks_on_fp8_code_pools_moves_whole_blocks_of_bytes():
+    """e4m3 code pools (one byte an element): the same block copy, byte for byte."""
+    rng = np.random.default_rng(6)
+    kp = rng.integers(0, 256, (5, 16, 8, 128), dtype=np.uint8)
+    vp = rng.integers(0, 256, (5, 16, 8, 128), dtype=np.uint8)
+    k0, v0 = kp.copy(), vp.copy()
+    oracle.copy_blocks(kp, vp, np.array([[3, 0], [0, 4]], np.int32), "fp8")   # 0 <- 3, 4 <- old 0
+    assert np.array_equal(kp[0], k0[3]) and np.array_equal(vp[0], v0[3])
+    assert np.array_equal(kp[4], k0[0]) and np.array_equal(vp[4], v0[0])
+    for blk in (1, 2, 3):
+        assert np.array_equal(kp[blk], k0[blk]) and np.array_equal(vp[blk], v0[blk])
+
+
 def test_copy_blocks_rejects_out_of_range_ids_before_writing():
     g = W.Geometry(H_q=4, H_kv=2, D=64, P=4, N=3, dtype=W.F32)
     kp, vp = W.empty_pool(g), W.empty_pool(g)
