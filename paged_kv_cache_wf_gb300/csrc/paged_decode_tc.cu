@@ -110,10 +110,6 @@ __device__ __forceinline__ uint32_t sw_elem(int row, int k, int block_bytes) {
                       ((chunk ^ (row & 7)) << 4) + (k & 7) * 2);
 }
 
-__device__ __forceinline__ bool tc_len_ok(int len, const TcParams& p) {
-    return len >= 1 && len <= p.max_seq_len && (int64_t)len <= (int64_t)p.M * p.P;
-}
-
 // 32 consecutive fp32 TMEM columns / 16 of them, this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) { tc::ld_32cols(taddr, v); }
 
@@ -183,31 +179,20 @@ __global__ void __launch_bounds__(192, 1)
         // ============================ producer ==================================
         const uint64_t pol = l2_policy_evict_first();
         int t = 0, k = 0;          // tiles and items issued
-        int b = 0, len = 0, nsp = -1;
+        int b = 0, len = 0, nsp = 0;
         int64_t cum = 0;
         bool ok = true;
+        const int64_t cap = min((int64_t)p.max_seq_len, (int64_t)p.M * p.P);   // longest valid sequence
+        ItemWalk walk;
+        item_walk_load(walk, p.seq_lens, p.B, kSpanTc, cap, p.dev_status, lane);
         // Items come from a queue shared by all CTAs (one atomic increment per item,
         // claimed one item ahead so the round trip overlaps the current item's
-        // copies).  Each CTA's claims increase, so the walk over sequences below
-        // only moves forward.
+        // copies).  Each CTA's claims increase, so its walk over the sequences only
+        // moves forward.
         uint32_t claim = lane == 0 ? atomicAdd(p.queue, 1u) : 0u;
         for (int64_t item = __shfl_sync(0xffffffffu, claim, 0); ok; item = __shfl_sync(0xffffffffu, claim, 0)) {
-            while (b < p.B) {
-                if (nsp < 0) {
-                    len = __ldg(p.seq_lens + b);
-                    if (tc_len_ok(len, p)) {
-                        nsp = (len + kSpanTc - 1) / kSpanTc;
-                    } else {
-                        nsp = 0;
-                        if (lane == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
-                    }
-                }
-                if (item < cum + nsp) break;
-                cum += nsp;
-                ++b;
-                nsp = -1;
-            }
-            if (b >= p.B) break;
+            if (!item_walk_find(walk, item, p.seq_lens, p.B, kSpanTc, cap, p.dev_status, lane, b, len, nsp, cum))
+                break;
             claim = lane == 0 ? atomicAdd(p.queue, 1u) : 0u;
             const int split = (int)(item - cum);
             const int s0 = split * kSpanTc;

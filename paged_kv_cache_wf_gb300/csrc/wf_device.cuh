@@ -92,6 +92,65 @@ __device__ __forceinline__ void e4m3x16_to_f16(const uint4& c, uint32_t (&w)[8])
     }
 }
 
+// Warp-cooperative walk from a work-item index to its (sequence, split).  A work
+// item is one split of `span` positions of one sequence, numbered sequence by
+// sequence.  The walk reads 32 sequences' lengths at once (lane l: sequence
+// base + l), prefix-sums their split counts across the warp and moves its window
+// forward only; callers ask for increasing item indices.  Lengths outside
+// [1, cap] count as zero splits and set WF_DEV_BAD_SEQLEN.
+struct ItemWalk {
+    int base = 0;       // first sequence of the window
+    int64_t cum = 0;    // items of the sequences before `base`
+    int len = 0;        // this lane's sequence length
+    int nsp = 0;        //   and its split count
+    int incl = 0;       // inclusive prefix of nsp over the window
+    int total = 0;      // items in the window
+};
+
+__device__ __forceinline__ void item_walk_load(ItemWalk& w, const int32_t* seq_lens, int B, int span, int64_t cap,
+                                               uint32_t* status, int lane) {
+    const int bb = w.base + lane;
+    int n = 0, len = 0;
+    if (bb < B) {
+        len = __ldg(seq_lens + bb);
+        if (len >= 1 && (int64_t)len <= cap) n = (len + span - 1) / span;
+        else report(status, WF_DEV_BAD_SEQLEN);
+    }
+    w.len = len;
+    w.nsp = n;
+    int x = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    w.incl = x;
+    w.total = __shfl_sync(0xffffffffu, x, 31);
+}
+
+// Finds item `item` (uniform across the warp): false when it lies past the last
+// sequence, else its sequence b, that sequence's length and split count, and the
+// number of items before the sequence.
+__device__ __forceinline__ bool item_walk_find(ItemWalk& w, int64_t item, const int32_t* seq_lens, int B, int span,
+                                               int64_t cap, uint32_t* status, int lane, int& b, int& len, int& nsp,
+                                               int64_t& cum) {
+    for (;;) {
+        if (w.base >= B) return false;
+        if (item < w.cum + w.total) {
+            const unsigned hit = __ballot_sync(0xffffffffu, w.cum + w.incl > item);
+            const int L = __ffs(hit) - 1;
+            b = w.base + L;
+            len = __shfl_sync(0xffffffffu, w.len, L);
+            nsp = __shfl_sync(0xffffffffu, w.nsp, L);
+            cum = w.cum + __shfl_sync(0xffffffffu, w.incl, L) - nsp;
+            return true;
+        }
+        w.cum += w.total;
+        w.base += 32;
+        if (w.base < B) item_walk_load(w, seq_lens, B, span, cap, status, lane);
+    }
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float y;
@@ -299,6 +358,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (the formats come from idesc).
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -325,6 +395,15 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_majo
            | ((uint32_t)b_mn_major << 16)  // B major-ness
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4)                       // D format: f32; A and B format 0: e4m3
+           | ((uint32_t)a_mn_major << 15)
+           | ((uint32_t)b_mn_major << 16)
+           | ((uint32_t)(N >> 3) << 17)
+           | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose

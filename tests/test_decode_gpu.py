@@ -206,3 +206,19 @@ def test_decode_workspace_left_dirty_is_fine_and_reusable(H_q, H_kv, D, P):
         outs.append(G.storage_bytes(out))
     assert np.array_equal(outs[0], outs[1])
     G.assert_close(G.from_dev(out, W.BF16), _oracle_decode(lay, vals, 0.088), W.BF16, "dirty workspace")
+
+
+def test_decode_tensor_core_path_flags_bad_seq_len():
+    """Llama-3-8B heads (tensor-core kernel): a sequence longer than max_seq_len is
+    skipped and flagged; the others are decoded as usual."""
+    lay = W.custom_layout(32, 8, 128, 16, W.BF16, [40, 50, 300, 60], seed=13)
+    vals = W.draw_layer_values(lay, np.random.default_rng(13))
+    kp, vp = G.build_dev_pools(lay, vals)
+    ref = _oracle_decode(lay, vals, 0.088)
+    bad = W.Layout(lay.geom, np.array([40, 50, 9999, 60], np.int32), lay.q_lens, lay.block_tables,
+                   lay.spare_block)
+    st = G.dev_status()
+    out = G.run_decode(bad, vals, (kp, vp), 0.088, st, max_seq_len=lay.max_seq_len)
+    assert wf.wf_device_status_fetch(st) == wf.WF_DEV_BAD_SEQLEN
+    got = G.from_dev(out, W.BF16)
+    G.assert_close(got[[0, 1, 3]], ref[[0, 1, 3]], W.BF16, "untouched sequences")

@@ -232,3 +232,22 @@ def test_fp8_copy_blocks_is_a_byte_copy():
     wf.wf_copy_blocks(dk, dv, torch.from_numpy(pairs).cuda(), k_scale=0.1, v_scale=0.1)
     oracle.copy_blocks(hk, hv, pairs, "fp8")
     assert np.array_equal(dk.cpu().numpy(), hk) and np.array_equal(dv.cpu().numpy(), hv)
+
+
+def test_fp8_decode_flags_bad_seq_len():
+    torch = G.torch_mod()
+    lay = W.custom_layout(32, 8, 128, 16, W.BF16, [40, 300, 60, 17], seed=31)
+    vals = W.draw_layer_values(lay, np.random.default_rng(31))
+    (dk, dv), (hk, hv) = _pools_both(lay, vals, 0.02, 0.02)
+    sl = lay.seq_lens.copy()
+    sl[1] = 9999                                          # > max_seq_len: skipped and flagged
+    q = G.to_dev(vals.q, W.BF16)
+    out = torch.zeros_like(q)
+    ws = torch.empty(wf.wf_paged_decode_workspace_size(lay.B, 32, lay.max_seq_len, wf.pool_desc(dk, 0.02, 0.02)),
+                     dtype=torch.uint8, device="cuda")
+    st = G.dev_status()
+    wf.wf_paged_decode(out, q, dk, dv, torch.from_numpy(lay.block_tables).cuda(), torch.from_numpy(sl).cuda(),
+                       lay.max_seq_len, 0.088, ws, st, k_scale=0.02, v_scale=0.02)
+    assert wf.wf_device_status_fetch(st) == wf.WF_DEV_BAD_SEQLEN
+    ref = oracle.paged_decode_fp8(vals.q, hk, hv, lay.block_tables, lay.seq_lens, 0.088, 0.02, 0.02)
+    G.assert_close(G.from_dev(out[[0, 2, 3]], W.BF16), ref[[0, 2, 3]], W.BF16, "sequences with good lengths")
