@@ -680,6 +680,8 @@ def main():
     total_ms, launch_ms = wl.timed(args.steps, per_launch=True)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    if wl.wf.wf_device_status_fetch(wl.status) != 0:
+        raise SystemExit("device status flagged an error during the timed steps")
     if pg is not None:
         t = torch.tensor([total_ms], device="cuda")
         pg.all_reduce(t, op=pg.ReduceOp.MAX)

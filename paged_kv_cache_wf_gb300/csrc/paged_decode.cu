@@ -689,7 +689,10 @@ size_t decode_workspace_bytes(int32_t B, int32_t num_q_heads, int32_t max_seq_le
     const int64_t rows = (int64_t)B * max_splits * num_q_heads;
     const int64_t o_bytes = rows * pool.head_dim * 4;
     const int64_t ml_bytes = rows * 8;
-    return (size_t)(((o_bytes + 255) / 256) * 256 + ml_bytes + 256);
+    const int64_t base = ((o_bytes + 255) / 256) * 256 + ml_bytes + 256;
+    // fp8 pools: the prepared q parts and row scales follow, 256-byte aligned
+    if (pool.dtype == WF_DTYPE_FP8_E4M3) return (size_t)((base + 255) / 256 * 256) + decode_fp8_prep_bytes(B, num_q_heads);
+    return (size_t)base;
 }
 
 cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -727,7 +730,8 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
     p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
     const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
     // the tensor-core kernels' work-item queue: one word after the (m, l) partials,
-    // inside the workspace's slack, zeroed on the stream before each launch
+    // inside the workspace's slack, zeroed on the stream before each launch (for fp8
+    // pools by the grid that prepares q)
     uint32_t* queue = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + o_bytes + (rows * 8 + 15) / 16 * 16);
     if (decode_tc_supported(pool, num_q_heads) && slots <= INT32_MAX) {
         cudaError_t err = cudaMemsetAsync(queue, 0, sizeof(uint32_t), stream);
@@ -741,11 +745,11 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
     if (pool.dtype == WF_DTYPE_FP8_E4M3) {
         // e4m3 pools have only the tensor-core path; the entry point rejects other shapes
         if (!decode_tc_fp8_supported(pool, num_q_heads) || slots > INT32_MAX) return cudaErrorInvalidValue;
-        cudaError_t err = cudaMemsetAsync(queue, 0, sizeof(uint32_t), stream);
-        if (err != cudaSuccess) return err;
-        err = launch_paged_decode_tc_fp8(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B,
-                                         max_seq_len, num_q_heads, scale, pool, p.ws_o, p.ws_ml, p.max_splits,
-                                         queue, dev_status, stream);
+        // the preparing grid zeroes the queue; its q parts follow the partials
+        void* prep = static_cast<char*>(workspace) + (o_bytes + rows * 8 + 256 + 255) / 256 * 256;
+        cudaError_t err = launch_paged_decode_tc_fp8(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                                                     seq_lens, B, max_seq_len, num_q_heads, scale, pool, p.ws_o,
+                                                     p.ws_ml, p.max_splits, queue, prep, dev_status, stream);
         if (err != cudaSuccess) return err;
         return p.max_splits > 1 ? launch_combine<BF16, 128>(p, stream) : cudaSuccess;
     }

@@ -29,10 +29,14 @@
 // A tile is two 16 KB boxes (K and V, one 128-byte swizzled row per (head,
 // position)), so a stage is half the bf16 kernel's and the ring holds five.
 //
+// A small grid runs first (fp8_q_prepare_kernel): it splits every q row into its
+// e4m3 parts once per call, into the workspace, and zeroes the work-item queue.  The
+// decode grid is its programmatic dependent: set-up overlaps, the producer waits.
+//
 // CTA (persistent, one per SM), 11 warps:
-//   warp 0   producer: claims items from the launch's queue; per item, splits the
-//            sequence's q into its e4m3 parts (lane n = q row n) in one of two q
-//            buffers; per tile, TMA copies of K and V (alternating lane pairs).
+//   warp 0   producer: claims items from the launch's queue; per item, a TMA copy
+//            of the sequence's q parts into one of two q buffers; per tile, TMA
+//            copies of K and V (alternating lane pairs) and the tile's meta.
 //   warp 1   S issuer: S(t) into one of two TMEM S buffers.
 //   warps 2-5  softmax of tile t (thread i = row i): P^T parts, and a record of the
 //            tile's rescale factors (and, at an item's end, l and m) in a ring.
@@ -65,7 +69,7 @@ constexpr int kThreadsFp8 = 352;
 
 struct Fp8Params {
     void* out;
-    const void* q;
+    const float* qinv;   // [B * H_q]: 2^-e of each prepared q row
     float* ws_o;
     float2* ws_ml;
     const int32_t* block_tables;
@@ -130,7 +134,7 @@ __device__ __forceinline__ void split2_e4m3(float x0, float x1, uint32_t& hi, ui
 template <int G>
 __global__ void __launch_bounds__(kThreadsFp8, 1)
     paged_decode_tc_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                               const Fp8Params p) {
+                               const __grid_constant__ CUtensorMap tm_q, const Fp8Params p) {
     constexpr int HQ = kHeads * G;                 // query heads (MMA N)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -191,6 +195,8 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
 
     if (warp == 0) {
         // ============================ producer ==================================
+        // the q parts, the row scales and the zeroed queue come from the preparing grid
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const uint64_t pol = l2_policy_evict_first();
         int t = 0, k = 0;          // tiles and items issued
         int b = 0, len = 0, nsp = 0;
@@ -218,53 +224,9 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
                 ok = false;
                 break;
             }
-            // q row `lane` of sequence b -> e4m3 hi and lo parts with scale 2^e
-            float qinv = 1.f;
-            if (lane < p.H_q) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.H_q + lane) * kD);
-                float amax = 0.f;                    // pass 1 over the row's 128 bf16 values
-#pragma unroll 4
-                for (int j = 0; j < 16; ++j) {
-                    const uint4 v = __ldg(src + j);
-                    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float2 f = bf16x2_to_float2(u4[h]);
-                        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-                    }
-                }
-                int e = 0;
-                if (amax > 0.f && amax <= 3.0e38f) {
-                    // floor(log2 amax) from the exponent bits (subnormals count as 2^-126)
-                    const int E = max(-126, (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127);
-                    e = min(126, max(-126, 7 - E));
-                }
-                const float qs = __uint_as_float((uint32_t)(e + 127) << 23);
-                qinv = __uint_as_float((uint32_t)(127 - e) << 23);
-                unsigned char* qd = smem + Fp8Smem::qbuf + qb * kPartsBytes;
-#pragma unroll 2
-                for (int j = 0; j < 8; ++j) {        // pass 2: 16 d values per 16-byte output chunk
-                    const uint4 va = __ldg(src + 2 * j), vb = __ldg(src + 2 * j + 1);
-                    const uint32_t wj[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-                    uint32_t hw[4], lw[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float2 f0 = bf16x2_to_float2(wj[2 * h]);
-                        const float2 f1 = bf16x2_to_float2(wj[2 * h + 1]);
-                        uint32_t h0, l0, h1, l1;
-                        float2 d0, d1;
-                        split2_e4m3(f0.x * qs, f0.y * qs, h0, l0, d0);
-                        split2_e4m3(f1.x * qs, f1.y * qs, h1, l1, d1);
-                        hw[h] = (h0 & 0xffffu) | (h1 << 16);
-                        lw[h] = (l0 & 0xffffu) | (l1 << 16);
-                    }
-                    *reinterpret_cast<uint4*>(qd + sw_chunk(lane, j)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(qd + kPart + sw_chunk(lane, j)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                }
-            }
-            tc::fence_proxy_async_smem();   // the MMAs read the q parts through the async proxy
-            __syncwarp();
+            // the sequence's q parts arrive by TMA with the item's first tile; its row
+            // scales travel in the tiles' meta
+            const float qinv = lane < p.H_q ? __ldg(p.qinv + (int64_t)b * p.H_q + lane) : 1.f;
             for (int j = 0; j < ntiles; ++j, ++t) {
                 const int st = t % kStages;
                 if (t >= kStages && !mbar_wait(&empty[st], ((t / kStages) - 1) & 1)) {
@@ -283,9 +245,14 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
                     Fp8Meta& m = meta[st];
                     m.b = b; m.split = split; m.nsplit = nsp; m.p0 = p0; m.nvalid = nvalid;
                     m.first = (j == 0); m.last = (j == ntiles - 1); m.item = k;
-                    mbar_arrive_expect_tx(&full[st], okb ? (uint32_t)kStageBytes : 0u);
+                    mbar_arrive_expect_tx(&full[st], (okb ? (uint32_t)kStageBytes : 0u) +
+                                                         (j == 0 ? 2u * (uint32_t)HQ * 128u : 0u));
                 }
                 __syncwarp();
+                if (j == 0 && (lane == 8 || lane == 9)) {   // hi rows, then lo rows
+                    tma_load_2d(smem + Fp8Smem::qbuf + qb * kPartsBytes + (lane - 8) * kPart, &tm_q, 0,
+                                (lane - 8) * p.B * p.H_q + b * p.H_q, &full[st]);
+                }
                 const int slot = blk * p.P + p0 % p.P;
                 const int base_lane = (t & 3) * 2;   // a thread's copies complete in order: rotate lanes
                 if (okb && (lane == base_lane || lane == base_lane + 1)) {
@@ -559,7 +526,48 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
     }
 }
 
+// q [rows = B * H_q, 128] bf16 -> the e4m3 parts of q 2^e_r: hi in rows [0, rows),
+// lo in rows [rows, 2 rows) of `parts` (128 bytes a row), and qinv[r] = 2^-e_r, with
+// e_r chosen so that the row's largest magnitude lands in [128, 256).  One warp per
+// row, lane l holding d = 4l .. 4l + 3.  Block 0 also zeroes the decode's work-item
+// queue.  Run once per call, so every split of a sequence reads the same parts.
+__global__ void __launch_bounds__(256) fp8_q_prepare_kernel(const __nv_bfloat16* __restrict__ q,
+                                                            unsigned char* __restrict__ parts,
+                                                            float* __restrict__ qinv, int64_t rows,
+                                                            uint32_t* queue) {
+    // the decode grid may start its set-up now; it waits for this grid before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0) *queue = 0u;
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const uint2 v = *reinterpret_cast<const uint2*>(q + r * kD + 4 * lane);
+    const float2 a = bf16x2_to_float2(v.x), c = bf16x2_to_float2(v.y);
+    float amax = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(c.x), fabsf(c.y)));
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, mask));
+    int e = 0;
+    if (amax > 0.f && amax <= 3.0e38f) {
+        // floor(log2 amax) from the exponent bits (subnormals count as 2^-126)
+        const int E = max(-126, (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127);
+        e = min(126, max(-126, 7 - E));
+    }
+    const float qs = __uint_as_float((uint32_t)(e + 127) << 23);
+    uint32_t h0, l0, h1, l1;
+    float2 u0, u1;
+    split2_e4m3(a.x * qs, a.y * qs, h0, l0, u0);
+    split2_e4m3(c.x * qs, c.y * qs, h1, l1, u1);
+    *reinterpret_cast<uint32_t*>(parts + r * 128 + 4 * lane) = (h0 & 0xffffu) | (h1 << 16);
+    *reinterpret_cast<uint32_t*>(parts + (rows + r) * 128 + 4 * lane) = (l0 & 0xffffu) | (l1 << 16);
+    if (lane == 0) qinv[r] = __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
 }  // namespace
+
+size_t decode_fp8_prep_bytes(int32_t B, int32_t num_q_heads) {
+    const int64_t rows = (int64_t)B * num_q_heads;
+    return (size_t)(2 * rows * 128 + rows * 4 + 256);
+}
 
 bool decode_tc_fp8_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
     const int G = pool.num_kv_heads > 0 ? num_q_heads / pool.num_kv_heads : 0;
@@ -571,10 +579,14 @@ cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_p
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                                        const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                                        int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
-                                       float2* ws_ml, int32_t max_splits, uint32_t* queue,
+                                       float2* ws_ml, int32_t max_splits, uint32_t* queue, void* prep,
                                        uint32_t* dev_status, cudaStream_t stream) {
     const int G = num_q_heads / pool.num_kv_heads;
-    CUtensorMap tm_k, tm_v;
+    const int64_t rows = (int64_t)B * num_q_heads;
+    // prep: the q parts (2 rows x 128 bytes per q row), then the row scales
+    unsigned char* parts = static_cast<unsigned char*>(prep);
+    float* qinv = reinterpret_cast<float*>(parts + 2 * rows * 128);
+    CUtensorMap tm_k, tm_v, tm_q;
     const uint64_t slots = (uint64_t)pool.num_blocks * pool.block_size;
     {
         // (d, slot, head) over the code pools: one box = 16 slots x 8 heads x 128 codes
@@ -587,9 +599,22 @@ cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_p
         e = encode_tiled(&tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(v_pool), 3, dims, strides, box);
         if (e != cudaSuccess) return e;
     }
+    {
+        // (d, part row): one box = one sequence's H_q rows of one part
+        const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)(2 * rows)};
+        const uint64_t strides[1] = {(uint64_t)kD};
+        const uint32_t box[2] = {(uint32_t)kD, (uint32_t)num_q_heads};
+        cudaError_t e = encode_tiled(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, parts, 2, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    fp8_q_prepare_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(q), parts, qinv, rows, queue);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
     Fp8Params p;
     p.out = out;
-    p.q = q;
+    p.qinv = qinv;
     p.ws_o = ws_o;
     p.ws_ml = ws_ml;
     p.block_tables = block_tables;
@@ -610,17 +635,23 @@ cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_p
     const int smem = Fp8Smem::total + 1024;
     const int64_t items = (int64_t)B * max_splits;
     const int grid = (int)(items < num_sms() ? items : num_sms());
-    cudaError_t err;
-    if (G == 4) {
-        err = allow_dynamic_smem((const void*)paged_decode_tc_fp8_kernel<4>, smem);
-        if (err != cudaSuccess) return err;
-        paged_decode_tc_fp8_kernel<4><<<grid, kThreadsFp8, smem, stream>>>(tm_k, tm_v, p);
-    } else {
-        err = allow_dynamic_smem((const void*)paged_decode_tc_fp8_kernel<2>, smem);
-        if (err != cudaSuccess) return err;
-        paged_decode_tc_fp8_kernel<2><<<grid, kThreadsFp8, smem, stream>>>(tm_k, tm_v, p);
-    }
-    return cudaGetLastError();
+    const void* kern = G == 4 ? (const void*)paged_decode_tc_fp8_kernel<4> : (const void*)paged_decode_tc_fp8_kernel<2>;
+    err = allow_dynamic_smem(kern, smem);
+    if (err != cudaSuccess) return err;
+    // launched as a programmatic dependent of the preparing grid: its set-up overlaps
+    // that grid, and its producer waits (griddepcontrol.wait) before reading anything
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsFp8);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (G == 4) return cudaLaunchKernelEx(&cfg, paged_decode_tc_fp8_kernel<4>, tm_k, tm_v, tm_q, p);
+    return cudaLaunchKernelEx(&cfg, paged_decode_tc_fp8_kernel<2>, tm_k, tm_v, tm_q, p);
 }
 
 }  // namespace wf

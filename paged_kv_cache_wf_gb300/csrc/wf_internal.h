@@ -75,8 +75,10 @@ cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_p
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                                        const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                                        int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
-                                       float2* ws_ml, int32_t max_splits, uint32_t* queue,
+                                       float2* ws_ml, int32_t max_splits, uint32_t* queue, void* prep,
                                        uint32_t* dev_status, cudaStream_t stream);
+// Workspace the fp8 decode needs beyond the partials: the prepared q parts and scales.
+size_t decode_fp8_prep_bytes(int32_t B, int32_t num_q_heads);
 
 // ---- prefill ------------------------------------------------------------------
 // Pipelined tcgen05 prefill (bf16, P % 16 == 0, G in {1, 2, 4, 8}, D in {64, 128}).
