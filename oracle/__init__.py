@@ -62,10 +62,10 @@ def _load():
             lib.wfo_e4m3_decode.restype = d
             lib.wfo_e4m3_encode.argtypes = [f]
             lib.wfo_e4m3_encode.restype = ctypes.c_uint8
-            lib.wfo_reshape_and_cache_fp8.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, f, f]
+            lib.wfo_reshape_and_cache_fp8.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, p, p]
             lib.wfo_reshape_and_cache_fp8.restype = i32
             lib.wfo_paged_decode_fp8.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, i64, i64, i64,
-                                                 d, f, f, i32]
+                                                 d, p, p, i32]
             lib.wfo_paged_decode_fp8.restype = i32
             lib.wfo_paged_decode.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, i64, i64, i64,
                                              d, i32, i32]
@@ -130,22 +130,34 @@ def e4m3_encode(y: float) -> int:
     return int(_load().wfo_e4m3_encode(float(y)))
 
 
-def reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale: float, v_scale: float):
-    """In-place scatter of bf16 rows into uint8 (e4m3 code) pools [N, P, H_kv, D]."""
+def head_scales(scale, H_kv: int) -> np.ndarray:
+    """A per-tensor scale (a number) or H_kv per-head scales -> float32 [H_kv]."""
+    a = np.asarray(scale, dtype=np.float32).reshape(-1)
+    if a.shape[0] == 1:
+        a = np.full(H_kv, a[0], np.float32)
+    assert a.shape[0] == H_kv, (a.shape, H_kv)
+    return np.ascontiguousarray(a)
+
+
+def reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale, v_scale):
+    """In-place scatter of bf16 rows into uint8 (e4m3 code) pools [N, P, H_kv, D];
+    k_scale, v_scale: one number or one scale per KV head."""
     lib = _load()
     assert k_pool.dtype == np.uint8 and k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
     N, P, H_kv, D = k_pool.shape
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     slots = _c(slot_mapping, np.int64)
+    ks, vs = head_scales(k_scale, H_kv), head_scales(v_scale, H_kv)
     _check(lib.wfo_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slots),
-                                         int(slots.shape[0]), N, P, H_kv, D, float(k_scale), float(v_scale)),
+                                         int(slots.shape[0]), N, P, H_kv, D, _ptr(ks), _ptr(vs)),
            "wfo_reshape_and_cache_fp8")
 
 
-def paged_decode_fp8(q, k_pool, v_pool, block_tables, seq_lens, scale: float, k_scale: float, v_scale: float,
+def paged_decode_fp8(q, k_pool, v_pool, block_tables, seq_lens, scale: float, k_scale, v_scale,
                      nthreads: int | None = None) -> np.ndarray:
-    """fp64 decode outputs [B, H_q, D] for bf16 q and e4m3-code pools."""
+    """fp64 decode outputs [B, H_q, D] for bf16 q and e4m3-code pools (k_scale, v_scale:
+    one number or one scale per KV head)."""
     lib = _load()
     q = _c(q, np.uint16)
     k_pool = _c(k_pool, np.uint8)
@@ -154,9 +166,10 @@ def paged_decode_fp8(q, k_pool, v_pool, block_tables, seq_lens, scale: float, k_
     sl = _c(seq_lens, np.int32)
     B, H_q, D = q.shape
     N, P, H_kv, _ = k_pool.shape
+    ks, vs = head_scales(k_scale, H_kv), head_scales(v_scale, H_kv)
     out = np.zeros((B, H_q, D), np.float64)
     _check(lib.wfo_paged_decode_fp8(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(bt), int(bt.shape[1]),
-                                    _ptr(sl), B, H_q, H_kv, D, N, P, float(scale), float(k_scale), float(v_scale),
+                                    _ptr(sl), B, H_q, H_kv, D, N, P, float(scale), _ptr(ks), _ptr(vs),
                                     nthreads or default_threads()), "wfo_paged_decode_fp8")
     return out
 

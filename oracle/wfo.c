@@ -93,24 +93,31 @@ int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_po
     return 0;
 }
 
-/* ---- scatter into an fp8 pool: code = e4m3(float(x) * (1 / scale)), with the
+static int scales_ok(const float* s, int64_t n) {
+    for (int64_t i = 0; i < n; ++i)
+        if (!(s[i] > 0.0f) || isinf(s[i])) return 0;
+    return 1;
+}
+
+/* ---- scatter into an fp8 pool: code = e4m3(float(x) * (1 / scale_h)), with the
  * reciprocal and the product rounded to float32 (the precision the device uses
- * for this decision); k, v are bfloat16 [T, H_kv, D] ------------------------ */
+ * for this decision); k, v are bfloat16 [T, H_kv, D]; scale_h is KV head h's
+ * scale (one per head; a per-tensor scale is the same value for every head) --- */
 int wfo_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v_pool,
                               const int64_t* slot_mapping, int64_t T, int64_t N, int64_t P,
-                              int64_t H_kv, int64_t D, float k_scale, float v_scale) {
-    if (T < 0 || N < 1 || P < 1 || H_kv < 1 || D < 1 || !(k_scale > 0.0f) || !(v_scale > 0.0f) ||
-        isinf(k_scale) || isinf(v_scale))
+                              int64_t H_kv, int64_t D, const float* k_scales, const float* v_scales) {
+    if (T < 0 || N < 1 || P < 1 || H_kv < 1 || D < 1 || !scales_ok(k_scales, H_kv) || !scales_ok(v_scales, H_kv))
         return WFO_ERR_ARG;
     for (int64_t t = 0; t < T; ++t)
         if (slot_mapping[t] >= N * P) return WFO_ERR_SLOT;
-    const float kinv = 1.0f / k_scale, vinv = 1.0f / v_scale;
     const int64_t row = H_kv * D;
     for (int64_t t = 0; t < T; ++t) {
         const int64_t slot = slot_mapping[t];
         if (slot < 0) continue;
         const int64_t dst = ((slot / P) * P + slot % P) * row;
         for (int64_t i = 0; i < row; ++i) {
+            const int64_t h = i / D;
+            const float kinv = 1.0f / k_scales[h], vinv = 1.0f / v_scales[h];
             const float xk = (float)load_elem(k, t * row + i, WFO_BF16);
             const float xv = (float)load_elem(v, t * row + i, WFO_BF16);
             volatile float yk = xk * kinv; /* one float32 rounding, no contraction */
@@ -163,7 +170,8 @@ typedef struct {
     double scale;
     int dtype;              /* of q (and of the pools unless kv_dtype says fp8) */
     int kv_dtype;
-    double k_scale, v_scale; /* dequantization: value = scale * stored value */
+    const float* k_scales;   /* fp8 pools: per KV head, value = scale * stored value; */
+    const float* v_scales;   /*   NULL: stored values are the values                */
     double* out;
     int64_t next;            /* shared work counter (atomic)       */
     int status;
@@ -179,6 +187,8 @@ static int attend_row(const job_t* J, int64_t row, int64_t g, double* s, double*
     const int64_t h = g / G;
     const int64_t qbase = (row * J->H_q + g) * J->D;
     const int32_t* table = J->block_tables + b * J->M;
+    const double ks = J->k_scales ? (double)J->k_scales[h] : 1.0;
+    const double vs = J->v_scales ? (double)J->v_scales[h] : 1.0;
     double m = -INFINITY;
     for (int64_t p = 0; p < len; ++p) {
         const int64_t block = table[p / J->P];
@@ -187,7 +197,7 @@ static int attend_row(const job_t* J, int64_t row, int64_t g, double* s, double*
         const int64_t kbase = ((block * J->P + offset) * J->H_kv + h) * J->D;
         double dot = 0.0;
         for (int64_t d = 0; d < J->D; ++d)
-            dot += load_elem(J->q, qbase + d, J->dtype) * (J->k_scale * load_elem(J->k_pool, kbase + d, J->kv_dtype));
+            dot += load_elem(J->q, qbase + d, J->dtype) * (ks * load_elem(J->k_pool, kbase + d, J->kv_dtype));
         s[p] = J->scale * dot;
         if (s[p] > m) m = s[p];
     }
@@ -200,7 +210,7 @@ static int attend_row(const job_t* J, int64_t row, int64_t g, double* s, double*
         const int64_t vbase = ((block * J->P + offset) * J->H_kv + h) * J->D;
         den += w;
         for (int64_t d = 0; d < J->D; ++d)
-            acc[d] += w * (J->v_scale * load_elem(J->v_pool, vbase + d, J->kv_dtype));
+            acc[d] += w * (vs * load_elem(J->v_pool, vbase + d, J->kv_dtype));
     }
     double* o = J->out + (row * J->H_q + g) * J->D;
     for (int64_t d = 0; d < J->D; ++d) o[d] = acc[d] / den;
@@ -267,8 +277,8 @@ static int check_common(const int32_t* block_tables, int64_t M, int64_t B, int64
 static int decode_impl(double* out, const void* q, const void* k_pool, const void* v_pool,
                        const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
                        int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
-                       double scale, int q_dtype, int kv_dtype, double k_scale, double v_scale,
-                       int nthreads) {
+                       double scale, int q_dtype, int kv_dtype, const float* k_scales,
+                       const float* v_scales, int nthreads) {
     int rc = check_common(block_tables, M, B, H_q, H_kv, D, N, P, q_dtype);
     if (rc) return rc;
     for (int64_t b = 0; b < B; ++b)
@@ -285,7 +295,7 @@ static int decode_impl(double* out, const void* q, const void* k_pool, const voi
         row_len[b] = seq_lens[b];
     }
     job_t J = {q, k_pool, v_pool, block_tables, seq_lens, row_req, row_len,
-               B, M, H_q, H_kv, D, N, P, scale, q_dtype, kv_dtype, k_scale, v_scale, out, 0, 0};
+               B, M, H_q, H_kv, D, N, P, scale, q_dtype, kv_dtype, k_scales, v_scales, out, 0, 0};
     rc = run_job(&J, nthreads);
     free(row_req);
     free(row_len);
@@ -297,16 +307,16 @@ int wfo_paged_decode(double* out, const void* q, const void* k_pool, const void*
                      int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
                      double scale, int dtype, int nthreads) {
     return decode_impl(out, q, k_pool, v_pool, block_tables, M, seq_lens, B, H_q, H_kv, D, N, P, scale,
-                       dtype, dtype, 1.0, 1.0, nthreads);
+                       dtype, dtype, NULL, NULL, nthreads);
 }
 
 int wfo_paged_decode_fp8(double* out, const void* q, const void* k_pool, const void* v_pool,
                          const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
                          int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
-                         double scale, float k_scale, float v_scale, int nthreads) {
-    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || isinf(k_scale) || isinf(v_scale)) return WFO_ERR_ARG;
+                         double scale, const float* k_scales, const float* v_scales, int nthreads) {
+    if (H_kv < 1 || !scales_ok(k_scales, H_kv) || !scales_ok(v_scales, H_kv)) return WFO_ERR_ARG;
     return decode_impl(out, q, k_pool, v_pool, block_tables, M, seq_lens, B, H_q, H_kv, D, N, P, scale,
-                       WFO_BF16, WFO_FP8, (double)k_scale, (double)v_scale, nthreads);
+                       WFO_BF16, WFO_FP8, k_scales, v_scales, nthreads);
 }
 
 /* ---- prefill (causal varlen over the cached prefix plus the new rows) --- */
@@ -339,7 +349,7 @@ int wfo_paged_prefill(double* out, const void* q, const void* k_pool, const void
         }
     }
     job_t J = {q, k_pool, v_pool, block_tables, seq_lens, row_req, row_len,
-               rows, M, H_q, H_kv, D, N, P, scale, dtype, dtype, 1.0, 1.0, out, 0, 0};
+               rows, M, H_q, H_kv, D, N, P, scale, dtype, dtype, NULL, NULL, out, 0, 0};
     rc = run_job(&J, nthreads);
     free(row_req);
     free(row_len);

@@ -51,18 +51,20 @@ int wfo_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_po
 double wfo_e4m3_decode(uint8_t code);
 uint8_t wfo_e4m3_encode(float y);
 
-/* Scatter into fp8 pools: k, v are bfloat16 [T, H_kv, D]; each element is stored
- * as e4m3(float(x) * (1.0f / scale)), the reciprocal and product rounded to float32.
- * A stored code c stands for scale * value(c). */
+/* Scatter into fp8 pools: k, v are bfloat16 [T, H_kv, D]; an element of KV head h
+ * is stored as e4m3(float(x) * (1.0f / scale[h])), the reciprocal and product
+ * rounded to float32.  A stored code c of head h stands for scale[h] * value(c).
+ * k_scales, v_scales: H_kv finite positive scales each. */
 int wfo_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v_pool,
                               const int64_t* slot_mapping, int64_t T, int64_t N, int64_t P,
-                              int64_t H_kv, int64_t D, float k_scale, float v_scale);
+                              int64_t H_kv, int64_t D, const float* k_scales, const float* v_scales);
 
-/* Decode over fp8 pools (q bfloat16): K_p = k_scale * value(code), V_p likewise. */
+/* Decode over fp8 pools (q bfloat16): K_p of head h = k_scales[h] * value(code),
+ * V_p likewise. */
 int wfo_paged_decode_fp8(double* out, const void* q, const void* k_pool, const void* v_pool,
                          const int32_t* block_tables, int64_t M, const int32_t* seq_lens,
                          int64_t B, int64_t H_q, int64_t H_kv, int64_t D, int64_t N, int64_t P,
-                         double scale, float k_scale, float v_scale, int nthreads);
+                         double scale, const float* k_scales, const float* v_scales, int nthreads);
 
 /* Copy-on-write block copy: for every pair i, block pairs[2i+1] of both pools
  * becomes a byte copy of block pairs[2i] as it was before the call (a pair list

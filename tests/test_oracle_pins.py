@@ -488,3 +488,50 @@ def test_fp8_decode_matches_brute_force_on_dequantized_values():
     assert np.max(np.abs(got - ref)) <= 1e-12
     swapped = oracle.paged_decode_fp8(vals.q, kp, vp, lay.block_tables, lay.seq_lens, scale, v_scale, k_scale)
     assert np.max(np.abs(swapped - ref)) > 1e-3
+
+
+def _deq_per_head(torch, rows, scales):
+    """rows [T, H_kv, D] bf16 bits -> scale_h * e4m3(float32(x) * float32(1/scale_h)), by torch."""
+    x = torch.from_numpy(W.bf16_bits_to_f32(rows))
+    inv = torch.tensor((np.float32(1.0) / np.asarray(scales, np.float32)).astype(np.float32)).view(1, -1, 1)
+    c = (x * inv).to(torch.float8_e4m3fn)
+    # the scales are float32 numbers (the pool descriptor's type), widened exactly
+    return c, c.double().numpy() * np.asarray(scales, np.float32).astype(np.float64).reshape(1, -1, 1)
+
+
+def test_fp8_per_head_scales_scatter_and_decode():
+    """One scale per KV head (the survey's per-head variant of the fp8 pool): head h's
+    codes are torch's e4m3 cast of x * float32(1/scale_h), decode equals the
+    contiguous brute force on the per-head dequantized values, equal per-head scales
+    reproduce the per-tensor result exactly, and swapping two heads' scales breaks it."""
+    torch = _torch()
+    ks, vs = [0.0625, 0.3], [0.25, 0.011]
+    lay, vals, kp, vp = _fp8_case(k_scale=ks, v_scale=vs)
+    g = lay.geom
+    for rows, slots, pool, sc in ((vals.k_new, lay.new_slots(), kp, ks), (vals.v_prefix, lay.prefix_slots(), vp, vs)):
+        want, _ = _deq_per_head(torch, rows, sc)
+        assert np.array_equal(pool.reshape(-1, g.H_kv, g.D)[slots], want.view(torch.uint8).numpy())
+    scale = 1.0 / math.sqrt(g.D)
+    got = oracle.paged_decode_fp8(vals.q, kp, vp, lay.block_tables, lay.seq_lens, scale, ks, vs)
+    q = W.storage_to_f64(vals.q, g.dtype)
+    cp, cq = lay.cu_prefix, lay.cu_q_lens
+    ref = np.zeros_like(got)
+    for b in range(lay.B):
+        K = np.concatenate([_deq_per_head(torch, vals.k_prefix[cp[b]:cp[b + 1]], ks)[1],
+                            _deq_per_head(torch, vals.k_new[cq[b]:cq[b + 1]], ks)[1]])
+        V = np.concatenate([_deq_per_head(torch, vals.v_prefix[cp[b]:cp[b + 1]], vs)[1],
+                            _deq_per_head(torch, vals.v_new[cq[b]:cq[b + 1]], vs)[1]])
+        for hq in range(g.H_q):
+            s = scale * (K[:, hq // g.G, :] @ q[b, hq])
+            w = np.exp(s - s.max())
+            ref[b, hq] = (w @ V[:, hq // g.G, :]) / w.sum()
+    assert np.max(np.abs(got - ref)) <= 1e-12
+    swapped = oracle.paged_decode_fp8(vals.q, kp, vp, lay.block_tables, lay.seq_lens, scale, ks[::-1], vs)
+    assert np.max(np.abs(swapped - ref)) > 1e-3
+    # equal per-head scales are the per-tensor pool, byte for byte and output for output
+    lay1, vals1, kp1, vp1 = _fp8_case(k_scale=0.0625, v_scale=0.25)
+    lay2, vals2, kp2, vp2 = _fp8_case(k_scale=[0.0625, 0.0625], v_scale=[0.25, 0.25])
+    assert np.array_equal(kp1, kp2) and np.array_equal(vp1, vp2)
+    a = oracle.paged_decode_fp8(vals1.q, kp1, vp1, lay1.block_tables, lay1.seq_lens, scale, 0.0625, 0.25)
+    c = oracle.paged_decode_fp8(vals2.q, kp2, vp2, lay2.block_tables, lay2.seq_lens, scale, [0.0625] * 2, [0.25] * 2)
+    assert np.array_equal(a, c)
