@@ -20,7 +20,8 @@
  *
  * Conventions for every call
  *   - Every pointer argument is DEVICE memory owned by the caller, dense and
- *     row-major as documented, 16-byte aligned.  The library allocates nothing,
+ *     row-major as documented, 16-byte aligned (the optional per-head fp8 scale
+ *     arrays inside wf_pool_desc are the one exception: small host arrays).  The library allocates nothing,
  *     keeps no per-call state, and never synchronises the stream (except
  *     wf_device_status_fetch).  Calls are asynchronous and stream-ordered.
  *   - q, k, v, pools and outputs all use the pool's dtype (float32 or bfloat16);
@@ -85,6 +86,13 @@ typedef struct wf_pool_desc {
                               Must be finite and > 0 for fp8; ignored
                               otherwise.                                  */
     float v_scale;         /* the same for V                              */
+    const float* k_head_scales; /* fp8 pools, optional: NULL, or host memory
+                              holding num_kv_heads scales (num_kv_heads <= 64),
+                              one per KV head, read during the call and not
+                              kept.  When set, codes of head h stand for
+                              k_head_scales[h] * value(c) and k_scale is not
+                              used.  Each must be finite and > 0.          */
+    const float* v_head_scales; /* the same for V                         */
 } wf_pool_desc;
 
 /*
@@ -97,8 +105,11 @@ typedef struct wf_pool_desc {
  *                 A negative slot means "padding token": nothing is written.
  *                 Two tokens with the same slot: one of them wins (unspecified).
  *   num_tokens    T >= 0 (0 is a no-op)
- * Pure byte copy: pool bytes equal the input bytes exactly.  Slots >= N*P are
- * skipped and flagged WF_DEV_BAD_SLOT.
+ * Pure byte copy: pool bytes equal the input bytes exactly.  fp8 pools: k, v are
+ * bfloat16 and each element of KV head h is stored as the e4m3 code of
+ * float(x) * (1.0f / scale_h) (scale_h = k_head_scales[h] if given, else
+ * k_scale; likewise for V), rounded to nearest even, saturated at +-448, NaN kept.
+ * Slots >= N*P are skipped and flagged WF_DEV_BAD_SLOT.
  */
 wf_status wf_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                const int64_t* slot_mapping, int32_t num_tokens,

@@ -35,7 +35,8 @@ EXPORTS = (
 class wf_pool_desc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+                ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("k_head_scales", ctypes.POINTER(ctypes.c_float)), ("v_head_scales", ctypes.POINTER(ctypes.c_float))]
 
 
 class WfError(RuntimeError):
@@ -112,9 +113,18 @@ def _check(fn: str, rc: int):
         raise WfError(fn, rc)
 
 
-def pool_desc(k_pool, k_scale: float = 1.0, v_scale: float = 1.0) -> wf_pool_desc:
+def _scale_arg(scale):
+    """A number -> (per-tensor value, None); a sequence -> (1.0, host float array)."""
+    if isinstance(scale, (int, float)):
+        return float(scale), None
+    vals = [float(x) for x in scale]
+    return 1.0, (ctypes.c_float * len(vals))(*vals)
+
+
+def pool_desc(k_pool, k_scale=1.0, v_scale=1.0) -> wf_pool_desc:
     """Pool geometry from a [N, P, H_kv, D] float32 / bfloat16 tensor, or a uint8
-    tensor of fp8 e4m3 codes (with its dequantization scales)."""
+    tensor of fp8 e4m3 codes with its dequantization scales: a number (per tensor)
+    or one scale per KV head."""
     import torch
     N, P, H_kv, D = k_pool.shape
     if k_pool.dtype == torch.float32:
@@ -125,7 +135,11 @@ def pool_desc(k_pool, k_scale: float = 1.0, v_scale: float = 1.0) -> wf_pool_des
         dt = WF_DTYPE_FP8_E4M3
     else:
         raise TypeError(f"unsupported pool dtype {k_pool.dtype}")
-    return wf_pool_desc(N, P, H_kv, D, dt, float(k_scale), float(v_scale))
+    ks, karr = _scale_arg(k_scale)
+    vs, varr = _scale_arg(v_scale)
+    d = wf_pool_desc(N, P, H_kv, D, dt, ks, vs, karr, varr)
+    d._keep = (karr, varr)   # the host arrays live as long as the descriptor
+    return d
 
 
 def _contig(*ts):
@@ -138,7 +152,7 @@ def _contig(*ts):
 # the C entry points, torch-tensor flavoured
 # ---------------------------------------------------------------------------
 def wf_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, dev_status=None, stream=None,
-                         k_scale: float = 1.0, v_scale: float = 1.0):
+                         k_scale=1.0, v_scale=1.0):
     """Scatter k, v [T, H_kv, D] into k_pool, v_pool [N, P, H_kv, D] via slot_mapping [T] int64
     (uint8 pools: fp8 e4m3 codes of bf16 k, v quantized with k_scale, v_scale)."""
     _contig(k, v, k_pool, v_pool, slot_mapping)
@@ -149,8 +163,8 @@ def wf_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, dev_status=None, st
     _check("wf_reshape_and_cache", rc)
 
 
-def wf_copy_blocks(k_pool, v_pool, block_pairs, dev_status=None, stream=None, k_scale: float = 1.0,
-                   v_scale: float = 1.0):
+def wf_copy_blocks(k_pool, v_pool, block_pairs, dev_status=None, stream=None, k_scale=1.0,
+                   v_scale=1.0):
     """Copy block src to block dst of both pools for every (src, dst) row of block_pairs [n, 2] int32."""
     _contig(k_pool, v_pool, block_pairs)
     lib = load()
@@ -164,7 +178,7 @@ def wf_paged_decode_workspace_size(B: int, num_q_heads: int, max_seq_len: int, d
 
 
 def wf_paged_decode(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len: int, scale: float,
-                    workspace, dev_status=None, stream=None, k_scale: float = 1.0, v_scale: float = 1.0):
+                    workspace, dev_status=None, stream=None, k_scale=1.0, v_scale=1.0):
     """out, q [B, H_q, D]; block_tables [B, M] int32; seq_lens [B] int32; workspace uint8 tensor."""
     _contig(out, q, k_pool, v_pool, block_tables, seq_lens)
     lib = load()

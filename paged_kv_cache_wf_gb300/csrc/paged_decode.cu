@@ -730,13 +730,11 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
     p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
     const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
     // the tensor-core kernels' work-item queue: one word after the (m, l) partials,
-    // inside the workspace's slack, zeroed on the stream before each launch (for fp8
-    // pools by the grid that prepares q)
+    // inside the workspace's slack, zeroed by a small grid that runs before each
+    // decode grid (for fp8 pools, the grid that prepares q)
     uint32_t* queue = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + o_bytes + (rows * 8 + 15) / 16 * 16);
     if (decode_tc_supported(pool, num_q_heads) && slots <= INT32_MAX) {
-        cudaError_t err = cudaMemsetAsync(queue, 0, sizeof(uint32_t), stream);
-        if (err != cudaSuccess) return err;
-        err = launch_paged_decode_tc(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B,
+        cudaError_t err = launch_paged_decode_tc(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B,
                                      max_seq_len, num_q_heads, scale, pool, p.ws_o, p.ws_ml, p.max_splits, queue,
                                      dev_status, stream);
         if (err != cudaSuccess) return err;

@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         // ============================ producer ==================================
+        // the queue is zeroed by the grid this one depends on
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const uint64_t pol = l2_policy_evict_first();
         int t = 0, k = 0;          // tiles and items issued
         int b = 0, len = 0, nsp = 0;
@@ -471,6 +473,13 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+// Zeroes the decode's work-item queue; the decode grid is launched as its
+// programmatic dependent.
+__global__ void decode_queue_reset_kernel(uint32_t* queue) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) *queue = 0u;
+}
+
 }  // namespace
 
 bool decode_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
@@ -528,17 +537,25 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
     const int smem = TcSmem::total + 1024;
     const int64_t items = (int64_t)B * max_splits;
     const int grid = (int)(items < num_sms() ? items : num_sms());
-    cudaError_t err;
-    if (G == 4) {
-        err = allow_dynamic_smem((const void*)paged_decode_tc_kernel<4>, smem);
-        if (err != cudaSuccess) return err;
-        paged_decode_tc_kernel<4><<<grid, 192, smem, stream>>>(tm_k, tm_v, tm_q, p);
-    } else {
-        err = allow_dynamic_smem((const void*)paged_decode_tc_kernel<2>, smem);
-        if (err != cudaSuccess) return err;
-        paged_decode_tc_kernel<2><<<grid, 192, smem, stream>>>(tm_k, tm_v, tm_q, p);
-    }
-    return cudaGetLastError();
+    decode_queue_reset_kernel<<<1, 32, 0, stream>>>(queue);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const void* kern = G == 4 ? (const void*)paged_decode_tc_kernel<4> : (const void*)paged_decode_tc_kernel<2>;
+    err = allow_dynamic_smem(kern, smem);
+    if (err != cudaSuccess) return err;
+    // a programmatic dependent of the reset: its set-up overlaps, its producer waits
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (G == 4) return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<4>, tm_k, tm_v, tm_q, p);
+    return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<2>, tm_k, tm_v, tm_q, p);
 }
 
 }  // namespace wf

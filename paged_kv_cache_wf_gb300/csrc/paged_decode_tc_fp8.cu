@@ -3,8 +3,9 @@
 // 16 and GQA groups of 2 or 4; q and outputs are bf16.
 //
 // What is computed (ember, "Deliberately out of scope": paged KV quantization; the
-// attention itself as in paged_decode_tc.cu): K_p = k_scale * value(code),
-// V_p = v_scale * value(code), out = softmax_p(scale * q.K_p) V_p.
+// attention itself as in paged_decode_tc.cu): K_p = k_scale_h * value(code),
+// V_p = v_scale_h * value(code) with the scales of KV head h (per head, or one per
+// tensor), out = softmax_p(scale * q.K_p) V_p.
 //
 // The stored codes feed the tensor cores as they are (kind::f8f6f4, e4m3 x e4m3 ->
 // fp32): nothing widens K or V.  The other operand of each product is split into
@@ -15,11 +16,11 @@
 //     the remainder fits lo's 4, so hi + lo is q 2^e_n exactly unless lo falls
 //     below the e4m3 normal range (error <= 2^-10 on a scale where the row's
 //     largest entry is >= 128).  S = K (hi + lo)^T takes two MMAs per k-step and
-//     2^-e_n, k_scale and the softmax scale fold into the exponent.
+//     2^-e_n, the row's K scale and the softmax scale fold into the exponent.
 //   - the softmax weights p in [0, 1] are written as hi + lo of 256 p the same way
 //     (about 8 significant bits, what the bf16 kernel keeps), and l sums exactly
 //     the hi + lo that the P.V product uses; the factor 256 cancels in o / l, and
-//     v_scale multiplies the result.
+//     the V scale of each query head's KV head multiplies its output column.
 //
 // Work split, tiles and the (m, l, o) partials are those of the bf16 kernel: a work
 // item is (sequence b, split of 128 positions), a tile is one 16-position run of a
@@ -77,8 +78,9 @@ struct Fp8Params {
     uint32_t* dev_status;
     uint32_t* queue;     // next unclaimed work item; zero at launch
     int32_t M, B, max_seq_len, H_q, H_kv, G, N, P, max_splits;
-    float scale_log2;   // softmax scale * log2(e) * k_scale
-    float v_scale;
+    float scale_log2;   // softmax scale * log2(e)
+    float k_head[kHeads];   // K scale of each KV head
+    float v_head[kHeads];   // V scale of each KV head
 };
 
 struct Fp8Meta {
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
             }
             float colscale[G];                     // softmax scale * log2(e) * k_scale * 2^-e_n
 #pragma unroll
-            for (int g = 0; g < G; ++g) colscale[g] = p.scale_log2 * ms.qinv[hk * G + g];
+            for (int g = 0; g < G; ++g) colscale[g] = p.scale_log2 * p.k_head[hk] * ms.qinv[hk * G + g];
 
             if (!mbar_wait(&s_full[sb], (t >> 1) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
             tc::fence_after_sync();
@@ -504,11 +506,12 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
                 if (rec.nsplit == 1) {
                     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (int64_t)rec.b * p.H_q * kD + i;
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c) dst[c * kD] = __float2bfloat16_rn(acc[c] * p.v_scale / rec.l[c]);
+                    for (int c = 0; c < HQ; ++c)
+                        dst[c * kD] = __float2bfloat16_rn(acc[c] * p.v_head[c / G] / rec.l[c]);
                 } else {
                     const int64_t base = ((int64_t)rec.b * p.max_splits + rec.split) * p.H_q;
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c) p.ws_o[(base + c) * kD + i] = acc[c] * p.v_scale;
+                    for (int c = 0; c < HQ; ++c) p.ws_o[(base + c) * kD + i] = acc[c] * p.v_head[c / G];
                     if (i < HQ) p.ws_ml[base + i] = make_float2(rec.m[i], rec.l[i]);
                 }
             }
@@ -630,8 +633,12 @@ cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_p
     p.N = pool.num_blocks;
     p.P = pool.block_size;
     p.max_splits = max_splits;
-    p.scale_log2 = scale * 1.4426950408889634f * pool.k_scale;
-    p.v_scale = pool.v_scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const HeadScales sc = head_scales(pool);
+    for (int h = 0; h < kHeads; ++h) {
+        p.k_head[h] = sc.k[h];
+        p.v_head[h] = sc.v[h];
+    }
     const int smem = Fp8Smem::total + 1024;
     const int64_t items = (int64_t)B * max_splits;
     const int grid = (int)(items < num_sms() ? items : num_sms());

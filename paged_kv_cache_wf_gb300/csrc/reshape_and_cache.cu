@@ -36,13 +36,19 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
 }
 
 // fp8 e4m3 pools (ember, "Deliberately out of scope": paged KV quantization): the
-// bf16 rows are quantized on the way in, code = e4m3(float(x) * inv_scale) with
-// round-to-nearest-even and saturation at +-448 (NaN stays NaN).  A thread writes
-// 16 codes (one 16-byte chunk of the pool row) from 32 bytes of input.
+// bf16 rows are quantized on the way in, code = e4m3(float(x) * inv_scale_h) with
+// round-to-nearest-even and saturation at +-448 (NaN stays NaN), inv_scale_h the
+// float32 reciprocal of KV head h's scale.  A thread writes 16 codes (one 16-byte
+// chunk of the pool row, inside one head since D % 16 == 0) from 32 bytes of input.
+struct InvScales {
+    float k[kMaxScaleHeads];
+    float v[kMaxScaleHeads];
+};
+
 __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k_pool,
     uint4* __restrict__ v_pool, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
-    int64_t num_slots, int row_chunks, float k_inv, float v_inv, uint32_t* dev_status) {
+    int64_t num_slots, int row_chunks, int head_chunks, const InvScales inv, uint32_t* dev_status) {
     const int64_t total = num_tokens * row_chunks;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -56,8 +62,11 @@ __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
         }
         const int64_t in = (t * row_chunks + c) * 2;   // 16 bf16 = two 16-byte chunks
         uint4 kq, vq;
-        quantize16_e4m3(ld_global_stream(k + in), ld_global_stream(k + in + 1), k_inv, kq);
-        quantize16_e4m3(ld_global_stream(v + in), ld_global_stream(v + in + 1), v_inv, vq);
+        // pools with more heads than the table carry one per-tensor scale (the entry
+        // point allows per-head scales only up to kMaxScaleHeads heads)
+        const int h = min(c / head_chunks, kMaxScaleHeads - 1);
+        quantize16_e4m3(ld_global_stream(k + in), ld_global_stream(k + in + 1), inv.k[h], kq);
+        quantize16_e4m3(ld_global_stream(v + in), ld_global_stream(v + in + 1), inv.v[h], vq);
         st_global_v4(k_pool + slot * row_chunks + c, kq);
         st_global_v4(v_pool + slot * row_chunks + c, vq);
     }
@@ -76,10 +85,15 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool,
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (pool.dtype == WF_DTYPE_FP8_E4M3) {
+        const HeadScales sc = head_scales(pool);
+        InvScales inv;
+        for (int h = 0; h < kMaxScaleHeads; ++h) {
+            inv.k[h] = 1.0f / sc.k[h];
+            inv.v[h] = 1.0f / sc.v[h];
+        }
         reshape_and_cache_fp8_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
             (const uint4*)k, (const uint4*)v, (uint4*)k_pool, (uint4*)v_pool, slot_mapping, num_tokens,
-            (int64_t)pool.num_blocks * pool.block_size, row_chunks, 1.0f / pool.k_scale, 1.0f / pool.v_scale,
-            dev_status);
+            (int64_t)pool.num_blocks * pool.block_size, row_chunks, pool.head_dim / 16, inv, dev_status);
         return cudaGetLastError();
     }
     reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, stream>>>(

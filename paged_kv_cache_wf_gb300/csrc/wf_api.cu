@@ -89,9 +89,17 @@ wf_status check_pool(const wf_pool_desc& pool) {
         return WF_ERR_INVALID_ARG;
     if (pool.dtype != WF_DTYPE_F32 && pool.dtype != WF_DTYPE_BF16 && pool.dtype != WF_DTYPE_FP8_E4M3)
         return WF_ERR_UNSUPPORTED;
-    if (pool.dtype == WF_DTYPE_FP8_E4M3 &&
-        !(pool.k_scale > 0.f && pool.v_scale > 0.f && pool.k_scale <= 3.0e38f && pool.v_scale <= 3.0e38f))
-        return WF_ERR_INVALID_ARG;
+    if (pool.dtype == WF_DTYPE_FP8_E4M3) {
+        auto ok = [](float x) { return x > 0.f && x <= 3.0e38f; };   // finite and positive (NaN fails)
+        if (pool.k_head_scales == nullptr && !ok(pool.k_scale)) return WF_ERR_INVALID_ARG;
+        if (pool.v_head_scales == nullptr && !ok(pool.v_scale)) return WF_ERR_INVALID_ARG;
+        if ((pool.k_head_scales || pool.v_head_scales) && pool.num_kv_heads > wf::kMaxScaleHeads)
+            return WF_ERR_UNSUPPORTED;
+        for (int h = 0; h < pool.num_kv_heads; ++h) {
+            if (pool.k_head_scales && !ok(pool.k_head_scales[h])) return WF_ERR_INVALID_ARG;
+            if (pool.v_head_scales && !ok(pool.v_head_scales[h])) return WF_ERR_INVALID_ARG;
+        }
+    }
     if (pool.head_dim != 64 && pool.head_dim != 128) return WF_ERR_UNSUPPORTED;
     const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
     if (slots > (int64_t)INT32_MAX * 64) return WF_ERR_INVALID_ARG;
@@ -108,7 +116,7 @@ wf_status from_cuda(cudaError_t e) {
 
 extern "C" {
 
-int wf_abi_version(void) { return 101; }
+int wf_abi_version(void) { return 102; }
 
 const char* wf_status_string(wf_status s) {
     switch (s) {

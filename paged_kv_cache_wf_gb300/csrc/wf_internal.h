@@ -77,6 +77,22 @@ cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_p
                                        int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
                                        float2* ws_ml, int32_t max_splits, uint32_t* queue, void* prep,
                                        uint32_t* dev_status, cudaStream_t stream);
+// fp8 pools: the scale of each KV head (the per-head arrays when given, else the
+// per-tensor scale for every head), read on the host and passed by value.
+constexpr int kMaxScaleHeads = 64;
+struct HeadScales {
+    float k[kMaxScaleHeads];
+    float v[kMaxScaleHeads];
+};
+inline HeadScales head_scales(const wf_pool_desc& pool) {
+    HeadScales s;
+    for (int h = 0; h < kMaxScaleHeads; ++h) {
+        const bool in = h < pool.num_kv_heads;
+        s.k[h] = in && pool.k_head_scales ? pool.k_head_scales[h] : pool.k_scale;
+        s.v[h] = in && pool.v_head_scales ? pool.v_head_scales[h] : pool.v_scale;
+    }
+    return s;
+}
 // Workspace the fp8 decode needs beyond the partials: the prepared q parts and scales.
 size_t decode_fp8_prep_bytes(int32_t B, int32_t num_q_heads);
 

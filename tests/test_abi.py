@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.wf_abi_version() == 101
+    assert lib.wf_abi_version() == 102
     for code in range(5):
         assert wf.status_string(code)
 
@@ -175,3 +175,35 @@ def test_fp8_pool_argument_checks(lib):
     pf = lib.wf_paged_prefill
     rc = pf(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 8, 8, 64, 32, 0.1, _fp8(), None, None)
     assert rc == wf.WF_ERR_UNSUPPORTED
+
+
+def test_fp8_per_head_scale_checks(lib):
+    """Per-head fp8 scales (host arrays of H_kv values) replace the per-tensor ones;
+    each must be finite and positive, and at most 64 heads may carry them."""
+    sc = lib.wf_reshape_and_cache
+
+    def desc(ks, vs, H=8, k_scale=0.0, v_scale=0.0):
+        d = _fp8(H=H, ks=k_scale, vs=v_scale)
+        karr = (ctypes.c_float * len(ks))(*ks) if ks is not None else None
+        varr = (ctypes.c_float * len(vs))(*vs) if vs is not None else None
+        d.k_head_scales = ctypes.cast(karr, ctypes.POINTER(ctypes.c_float)) if karr is not None else None
+        d.v_head_scales = ctypes.cast(varr, ctypes.POINTER(ctypes.c_float)) if varr is not None else None
+        d._keep = (karr, varr)
+        return d
+
+    good = [0.01 * (h + 1) for h in range(8)]
+    assert sc(None, None, None, None, None, 0, desc(good, good), None, None) == wf.WF_OK      # per-tensor unused
+    assert sc(None, None, None, None, None, 0, desc(good, None), None, None) == wf.WF_ERR_INVALID_ARG  # v_scale 0
+    assert sc(None, None, None, None, None, 0, desc(good, None, v_scale=0.5), None, None) == wf.WF_OK
+    bad = list(good)
+    bad[5] = 0.0
+    assert sc(None, None, None, None, None, 0, desc(bad, good), None, None) == wf.WF_ERR_INVALID_ARG
+    bad[5] = float("nan")
+    assert sc(None, None, None, None, None, 0, desc(good, bad), None, None) == wf.WF_ERR_INVALID_ARG
+    wide = [0.5] * 80
+    assert sc(None, None, None, None, None, 0, desc(wide, wide, H=80), None, None) == wf.WF_ERR_UNSUPPORTED
+    assert sc(None, None, None, None, None, 0, _fp8(H=80), None, None) == wf.WF_OK           # per-tensor: any H
+    # the binding builds the arrays from a sequence
+    import torch
+    d = wf.pool_desc(torch.empty((2, 16, 8, 128), dtype=torch.uint8), good, 0.25)
+    assert d.dtype == wf.WF_DTYPE_FP8_E4M3 and abs(d.k_head_scales[7] - 0.08) < 1e-7 and not d.v_head_scales

@@ -251,3 +251,50 @@ def test_fp8_decode_flags_bad_seq_len():
     assert wf.wf_device_status_fetch(st) == wf.WF_DEV_BAD_SEQLEN
     ref = oracle.paged_decode_fp8(vals.q, hk, hv, lay.block_tables, lay.seq_lens, 0.088, 0.02, 0.02)
     G.assert_close(G.from_dev(out[[0, 2, 3]], W.BF16), ref[[0, 2, 3]], W.BF16, "sequences with good lengths")
+
+
+# one scale per KV head: spread over three octaves and not powers of two
+K_HEAD = [1 / 64 * (1.37 ** (h - 4)) for h in range(8)]
+V_HEAD = [1 / 96 * (0.71 ** (h - 3)) for h in range(8)]
+
+
+def test_fp8_per_head_scatter_bit_exact():
+    torch = G.torch_mod()
+    T, N, P = 200, 20, 16
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((2, T, 8, 128)).astype(np.float32)
+    x[:, ::9] *= 40.0                                   # saturate some codes in the small-scale heads
+    k, v = W.f32_to_bf16_bits(x[0]), W.f32_to_bf16_bits(x[1])
+    slots = rng.permutation(N * P)[:T].astype(np.int64)
+    g = W.Geometry(H_q=8, H_kv=8, D=128, P=P, N=N, dtype=W.BF16)
+    hk, hv = _empty_codes(g), _empty_codes(g)
+    dk, dv = _dev_u8(hk), _dev_u8(hv)
+    st = G.dev_status()
+    wf.wf_reshape_and_cache(G.to_dev(k, W.BF16), G.to_dev(v, W.BF16), dk, dv, torch.from_numpy(slots).cuda(), st,
+                            k_scale=K_HEAD, v_scale=V_HEAD)
+    oracle.reshape_and_cache_fp8(k, v, hk, hv, slots, K_HEAD, V_HEAD)
+    assert np.array_equal(dk.cpu().numpy(), hk) and np.array_equal(dv.cpu().numpy(), hv)
+    assert wf.wf_device_status_fetch(st) == 0
+
+
+@pytest.mark.parametrize("name", ["gqa4_ragged", "gqa2_P32"])
+def test_fp8_per_head_decode_matches_oracle(name):
+    torch = G.torch_mod()
+    lay = CASES[name]()
+    vals = W.draw_layer_values(lay, np.random.default_rng(43))
+    g = lay.geom
+    scale = G.default_scale(g.D)
+    st = G.dev_status()
+    (dk, dv), (hk, hv) = _pools_both(lay, vals, K_HEAD, V_HEAD, st)
+    assert np.array_equal(dk.cpu().numpy(), hk) and np.array_equal(dv.cpu().numpy(), hv)
+    q = G.to_dev(vals.q, W.BF16)
+    out = torch.empty_like(q)
+    ws = torch.empty(wf.wf_paged_decode_workspace_size(lay.B, g.H_q, lay.max_seq_len,
+                                                       wf.pool_desc(dk, K_HEAD, V_HEAD)),
+                     dtype=torch.uint8, device="cuda")
+    wf.wf_paged_decode(out, q, dk, dv, torch.from_numpy(lay.block_tables).cuda(),
+                       torch.from_numpy(lay.seq_lens).cuda(), lay.max_seq_len, scale, ws, st,
+                       k_scale=K_HEAD, v_scale=V_HEAD)
+    assert wf.wf_device_status_fetch(st) == 0
+    ref = oracle.paged_decode_fp8(vals.q, hk, hv, lay.block_tables, lay.seq_lens, scale, K_HEAD, V_HEAD)
+    G.assert_close(G.from_dev(out, W.BF16), ref, W.BF16, f"fp8 per-head {name}")
