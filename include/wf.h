@@ -50,7 +50,8 @@ typedef enum wf_status {
     WF_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, H_q % H_kv != 0 */
     WF_ERR_UNSUPPORTED = 2,  /* dtype / head_dim / group size this build does not handle     */
     WF_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the *_workspace_size value */
-    WF_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed                  */
+    WF_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed                  */
+    WF_ERR_NO_BLOCKS = 5     /* block manager: not enough free blocks (nothing was changed)  */
 } wf_status;
 
 typedef enum wf_dtype {

@@ -14,11 +14,11 @@ import threading
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libwf.so")
 
-WF_OK, WF_ERR_INVALID_ARG, WF_ERR_UNSUPPORTED, WF_ERR_WORKSPACE, WF_ERR_CUDA = range(5)
+WF_OK, WF_ERR_INVALID_ARG, WF_ERR_UNSUPPORTED, WF_ERR_WORKSPACE, WF_ERR_CUDA, WF_ERR_NO_BLOCKS = range(6)
 WF_DTYPE_F32, WF_DTYPE_BF16, WF_DTYPE_FP8_E4M3 = 0, 1, 2
 WF_DEV_BAD_SLOT, WF_DEV_BAD_BLOCK, WF_DEV_BAD_SEQLEN, WF_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
-# every entry point include/wf.h declares
+# every entry point include/*.h declares
 EXPORTS = (
     "wf_reshape_and_cache",
     "wf_copy_blocks",
@@ -29,6 +29,15 @@ EXPORTS = (
     "wf_device_status_fetch",
     "wf_status_string",
     "wf_abi_version",
+    "wf_bm_create",
+    "wf_bm_destroy",
+    "wf_bm_num_free",
+    "wf_bm_seq_len",
+    "wf_bm_ref_count",
+    "wf_bm_append",
+    "wf_bm_fork",
+    "wf_bm_free",
+    "wf_bm_tables",
 )
 
 
@@ -80,6 +89,25 @@ def load(path: str = LIB_PATH):
         lib.wf_status_string.restype = ctypes.c_char_p
         lib.wf_abi_version.argtypes = []
         lib.wf_abi_version.restype = ctypes.c_int
+        u64 = ctypes.c_uint64
+        lib.wf_bm_create.argtypes = [i32, i32, u64, ctypes.POINTER(vp)]
+        lib.wf_bm_create.restype = ctypes.c_int
+        lib.wf_bm_destroy.argtypes = [vp]
+        lib.wf_bm_destroy.restype = None
+        lib.wf_bm_num_free.argtypes = [vp]
+        lib.wf_bm_num_free.restype = i32
+        lib.wf_bm_seq_len.argtypes = [vp, i64]
+        lib.wf_bm_seq_len.restype = i64
+        lib.wf_bm_ref_count.argtypes = [vp, i32]
+        lib.wf_bm_ref_count.restype = i32
+        lib.wf_bm_append.argtypes = [vp, i64, i32, vp, vp, vp]
+        lib.wf_bm_append.restype = ctypes.c_int
+        lib.wf_bm_fork.argtypes = [vp, i64, i64]
+        lib.wf_bm_fork.restype = ctypes.c_int
+        lib.wf_bm_free.argtypes = [vp, i64]
+        lib.wf_bm_free.restype = ctypes.c_int
+        lib.wf_bm_tables.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+        lib.wf_bm_tables.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -231,3 +259,69 @@ def wf_device_status_fetch(dev_status, clear: bool = True, stream=None) -> int:
                                     _stream(stream))
     _check("wf_device_status_fetch", rc)
     return int(host.value)
+
+
+# ---------------------------------------------------------------------------
+# host-side block manager (include/wf_blocks.h)
+# ---------------------------------------------------------------------------
+class BlockManager:
+    """Blocks of one pool handed out to growing sequences, with reference-counted
+    prefix sharing and copy-on-write of shared, partly filled blocks."""
+
+    def __init__(self, num_blocks: int, block_size: int, shuffle_seed: int = 0):
+        import numpy as np
+        self._np = np
+        self.lib = load()
+        h = ctypes.c_void_p()
+        _check("wf_bm_create", self.lib.wf_bm_create(int(num_blocks), int(block_size), int(shuffle_seed),
+                                                      ctypes.byref(h)))
+        self.h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if self.h:
+            self.lib.wf_bm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return int(self.lib.wf_bm_num_free(self.h))
+
+    def seq_len(self, seq: int) -> int:
+        return int(self.lib.wf_bm_seq_len(self.h, int(seq)))
+
+    def ref_count(self, block: int) -> int:
+        return int(self.lib.wf_bm_ref_count(self.h, int(block)))
+
+    def append(self, seq: int, n: int):
+        """Slots (int64 [n]) of n new tokens of `seq`, and the copy-on-write pair
+        (src, dst) to copy before writing them, or None."""
+        np = self._np
+        slots = np.zeros(max(int(n), 1), np.int64)
+        pair = np.zeros(2, np.int32)
+        ncow = ctypes.c_int32(0)
+        _check("wf_bm_append", self.lib.wf_bm_append(self.h, int(seq), int(n), slots.ctypes.data,
+                                                      pair.ctypes.data, ctypes.byref(ncow)))
+        return slots[:int(n)], (tuple(int(x) for x in pair) if ncow.value else None)
+
+    def fork(self, parent: int, child: int):
+        _check("wf_bm_fork", self.lib.wf_bm_fork(self.h, int(parent), int(child)))
+
+    def free(self, seq: int):
+        _check("wf_bm_free", self.lib.wf_bm_free(self.h, int(seq)))
+
+    def tables(self, seqs, M: int, pad_block: int):
+        """block_tables int32 [B, M] and seq_lens int32 [B] of the sequences `seqs`."""
+        np = self._np
+        ids = np.ascontiguousarray(np.asarray(seqs, np.int64))
+        B = int(ids.shape[0])
+        bt = np.zeros((max(B, 1), int(M)), np.int32)
+        sl = np.zeros(max(B, 1), np.int32)
+        _check("wf_bm_tables", self.lib.wf_bm_tables(self.h, ids.ctypes.data, B, int(M), int(pad_block),
+                                                      bt.ctypes.data, sl.ctypes.data))
+        return bt[:B], sl[:B]

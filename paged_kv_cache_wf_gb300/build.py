@@ -52,12 +52,12 @@ def _compile(src: str, obj: str, verbose: bool) -> str:
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link libwf.so; returns its path."""
     os.makedirs(BUILD, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     newest_header = max([os.path.getmtime(h) for h in _headers()] + [0])
     jobs = []
     objs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         stale = (force or not os.path.exists(obj)
                  or os.path.getmtime(obj) < max(os.path.getmtime(src), newest_header))

@@ -125,6 +125,7 @@ const char* wf_status_string(wf_status s) {
         case WF_ERR_UNSUPPORTED: return "unsupported configuration";
         case WF_ERR_WORKSPACE: return "workspace missing or too small";
         case WF_ERR_CUDA: return "CUDA error";
+        case WF_ERR_NO_BLOCKS: return "not enough free blocks";
     }
     return "unknown status";
 }

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.wf_abi_version() == 102
-    for code in range(5):
+    for code in range(6):
         assert wf.status_string(code)
 
 
