@@ -202,7 +202,10 @@ class DecodeWorkload:
         self.scale = 1.0 / math.sqrt(g.D)
         self.stream = torch.cuda.current_stream()
         self.sp = self.stream.cuda_stream
-        self.launches_per_layer = 2 + (1 if -(-self.max_seq_len // self.split_span()) > 1 else 0)
+        # scatter, the grid that zeroes the work queue (fp8: and prepares q), the
+        # split kernel, and the combine when any sequence has more than one split
+        tc = g.H_kv == 8 and g.D == 128 and g.P % 16 == 0 and g.H_q // g.H_kv in (2, 4)
+        self.launches_per_layer = (3 if tc else 2) + (1 if -(-self.max_seq_len // self.split_span()) > 1 else 0)
 
     def split_span(self) -> int:
         return 128
@@ -351,7 +354,7 @@ class MixedWorkload:
         self.scale = 1.0 / math.sqrt(g.D)
         self.stream = torch.cuda.current_stream()
         self.sp = self.stream.cuda_stream
-        self.launches_per_layer = 1 + 1 + 2
+        self.launches_per_layer = 1 + 1 + 3   # scatter, prefill, queue reset + decode + combine
 
     def layer(self, l, ev=None):
         kp, vp = self.pools[l]
