@@ -12,7 +12,8 @@ against the measured HBM copy bandwidth, an end-to-end figure through host
 buffers, the oracle's CPU time on a bounded sample, launch count and clocks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--batch 118|231]
-                    [--workload llama8b|mixed] [--impl wf|reference]
+                    [--workload llama8b|gpt2|llama1b|mixed|cow] [--kv bf16|fp8]
+                    [--impl wf|reference] [--no-graph]
 
 Under torchrun each rank runs its own replica on its own GPU (no data-path
 collective; sequences are independent) and the slowest rank's time counts.
@@ -271,6 +272,36 @@ class DecodeWorkload:
         total_ms = start.elapsed_time(end)
         launch_ms = [a.elapsed_time(b) for a, b in self._ev_done] if per_launch else []
         return total_ms, launch_ms
+
+
+def graph_timed(wl, steps: int) -> float:
+    """The workload's step captured once as a CUDA graph (on a side stream, as
+    torch requires) and replayed: ms per replayed step, CUDA events around
+    `steps` replays after three warm-up replays."""
+    torch = wl.torch
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(wl.stream)
+    eager_sp = wl.sp
+    with torch.cuda.stream(side):
+        wl.sp = side.cuda_stream           # every call of the step goes to the capture stream
+        try:
+            with torch.cuda.graph(graph, stream=side):
+                wl.step()
+        finally:
+            wl.sp = eager_sp
+    wl.stream.wait_stream(side)
+    with torch.cuda.stream(wl.stream):
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(wl.stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(wl.stream)
+        end.synchronize()
+    return start.elapsed_time(end) / steps
 
 
 class E2EDecode:
@@ -627,6 +658,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip timing the step captured as one CUDA graph (reported under 'graph')")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run this many layers instead of the model's (recorded in config)")
     args = ap.parse_args()
@@ -702,6 +735,19 @@ def main():
     step_bytes = L * (dbytes + scatter_bytes(lay.B, g, kvb))
     traffic = recorded_traffic("paged_decode_fp8" if fp8 else "paged_decode", wname)
 
+    # ---- the same step as one replayed CUDA graph ---------------------------------------
+    graph = None
+    if not args.no_graph:
+        g_ms = graph_timed(wl, args.steps)
+        if pg is not None:
+            t = torch.tensor([g_ms], device="cuda")
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            g_ms = float(t.item())
+        if wl.wf.wf_device_status_fetch(wl.status) != 0:
+            raise SystemExit("device status flagged an error during the graph replays")
+        graph = {"value": world * lay.B * L / (g_ms / 1e3), "unit": UNIT, "ms_per_step": g_ms,
+                 "note": "the step (scatter + decode for every layer) captured once as a CUDA graph and replayed"}
+
     # ---- end to end through host buffers --------------------------------------------
     e2e = None
     if not args.no_e2e:
@@ -751,6 +797,7 @@ def main():
                          "pct_of_nominal_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "graph": graph,
             "gpu_launches": args.steps * L * wl.launches_per_layer,
             "clocks": clk,
         }
