@@ -205,7 +205,7 @@ class DecodeWorkload:
         self.sp = self.stream.cuda_stream
         # scatter, the grid that zeroes the work queue (fp8: and prepares q), the
         # split kernel, and the combine when any sequence has more than one split
-        tc = g.H_kv == 8 and g.D == 128 and g.P % 16 == 0 and g.H_q // g.H_kv in (2, 4)
+        tc = g.H_kv == 8 and g.D in (64, 128) and g.P % 16 == 0 and g.H_q // g.H_kv in (2, 4)
         self.launches_per_layer = (3 if tc else 2) + (1 if -(-self.max_seq_len // self.split_span()) > 1 else 0)
 
     def split_span(self) -> int:

@@ -1,6 +1,6 @@
 // paged_decode_tc.cu -- paged decode on the 5th-generation tensor cores, for bf16
-// pools with H_kv = 8 KV heads, D = 128, a block size that is a multiple of 16
-// and GQA groups of 2 or 4 (H_q = 16 or 32).
+// pools with H_kv = 8 KV heads, D = 64 or 128, a block size that is a multiple of
+// 16 and GQA groups of 2 or 4 (H_q = 16 or 32).
 //
 // Same contract and split-K structure as the CUDA-core decode in
 // paged_decode.cu (ember, "The core idea"; tiny-vllm-py, "KV Cache"; weft,
@@ -12,8 +12,10 @@
 // CUDA cores that instruction stream, not HBM, limits decode.  Here a tile is one
 // 16-position run of a block for all 8 KV heads -- 128 rows r = (head, position)
 // -- and the group's work is two dense products issued by one thread:
-//     S^T[128 rows x H_q]  = K[128 rows x 128 d] . Q^T[128 d x H_q]
+//     S^T[128 rows x H_q]  = K[128 rows x D] . Q^T[D x H_q]
 //     O^T[128 d x H_q]     = V^T[128 d x 128 rows] . P^T[128 rows x H_q]
+// (at D = 64 the upper 64 rows of V^T read a zero tile: same MMA shape, zero rows
+// of O^T that nobody stores)
 // with bf16 operands and fp32 accumulators in tensor memory.  Row r only belongs
 // to the G query heads of its KV head: S entries outside that diagonal block are
 // ignored and P^T is block-diagonal (its off-diagonal entries stay zero).
@@ -50,14 +52,10 @@ constexpr int kRows = 128;       // MMA M: 8 heads x 16 positions (and D = 128 f
 constexpr int kHeads = 8;        // KV heads per tile
 constexpr int kPosT = 16;        // positions per tile
 constexpr int kSpanTc = 128;     // positions per item (split)
-constexpr int kD = 128;
 constexpr int kNq = 32;          // max H_q handled (MMA N, padded to a multiple of 16)
-constexpr int kStages = 3;
 constexpr int kEndTile = -1;
 constexpr int kHalf = kRows * 128;             // one 64-wide half of a K or V tile: 16 KB
-constexpr int kStageBytes = 4 * kHalf;         // K0 K1 V0 V1
-constexpr int kQHalf = kNq * 128;              // one half of q: 32 rows x 128 B
-constexpr int kQBytes = 2 * kQHalf;
+constexpr int kQHalf = kNq * 128;              // one 64-wide half of q: 32 rows x 128 B
 constexpr int kPHalf = kNq * 128;              // one 64-row half of P^T (32 q rows x 128 B)
 constexpr int kPBytes = 2 * kPHalf;
 
@@ -77,12 +75,21 @@ struct TcMeta {
     int32_t b, split, nsplit, p0, nvalid, first, last, item;
 };
 
-struct TcSmem {  // byte offsets from the 1024-aligned base
+// Per head dimension D (64 or 128): a K or V tile is D/64 halves of 64 columns
+// (16 KB each).  At D = 64 the P.V product still runs as M = 128 rows of V^T, the
+// upper 64 of which read a zero half, so one MMA shape and TMEM layout serve both.
+template <int D>
+struct TcSmemT {  // byte offsets from the 1024-aligned base
+    static constexpr int NH = D / 64;
+    static constexpr int kStages = D == 128 ? 3 : 5;
+    static constexpr int kStageBytes = 2 * NH * kHalf;     // K halves, then V halves
+    static constexpr int kQBytes = NH * kQHalf;
     static constexpr int stage = 0;
-    static constexpr int qbuf = kStages * kStageBytes;
+    static constexpr int zero = kStages * kStageBytes;      // D = 64: V^T rows 64..127
+    static constexpr int qbuf = zero + (D == 64 ? kHalf : 0);
     static constexpr int pbuf = qbuf + 2 * kQBytes;
     static constexpr int bars = pbuf + 2 * kPBytes;
-    // full[3] empty[3] s_full[2] s_free[2] p_full[2] o_full[2] o_free[2] q_free[2] grp
+    // full[S] empty[S] s_full[2] s_free[2] p_full[2] o_full[2] o_free[2] q_free[2] grp
     static constexpr int nbars = 2 * kStages + 13;
     static constexpr int meta = (bars + nbars * 8 + 15) / 16 * 16;   // alpha/l/m below are read as float4
     static constexpr int alpha = meta + kStages * (int)sizeof(TcMeta);  // [3][kNq]: tile t in t % 3
@@ -91,15 +98,20 @@ struct TcSmem {  // byte offsets from the 1024-aligned base
     static constexpr int tmem_slot = mbuf + 3 * kNq * 4;
     static constexpr int total = tmem_slot + 16;
 };
-static_assert(TcSmem::total + 1024 <= 232448, "tensor-core decode exceeds shared memory");
-static_assert(TcSmem::alpha % 16 == 0 && TcSmem::lbuf % 16 == 0 && TcSmem::mbuf % 16 == 0,
+static_assert(TcSmemT<128>::total + 1024 <= 232448 && TcSmemT<64>::total + 1024 <= 232448,
+              "tensor-core decode exceeds shared memory");
+static_assert(TcSmemT<128>::alpha % 16 == 0 && TcSmemT<128>::lbuf % 16 == 0 && TcSmemT<128>::mbuf % 16 == 0 &&
+                  TcSmemT<64>::alpha % 16 == 0 && TcSmemT<64>::lbuf % 16 == 0 && TcSmemT<64>::mbuf % 16 == 0,
               "alpha, l and m buffers are read with 16-byte loads");
+static_assert(TcSmemT<64>::zero % 1024 == 0 && TcSmemT<64>::qbuf % 1024 == 0, "swizzle atoms stay 1024-aligned");
 
+template <int D>
 __device__ __forceinline__ unsigned char* stage_k(unsigned char* base, int st, int c) {
-    return base + TcSmem::stage + st * kStageBytes + c * kHalf;
+    return base + TcSmemT<D>::stage + st * TcSmemT<D>::kStageBytes + c * kHalf;
 }
+template <int D>
 __device__ __forceinline__ unsigned char* stage_v(unsigned char* base, int st, int c) {
-    return base + TcSmem::stage + st * kStageBytes + 2 * kHalf + c * kHalf;
+    return base + TcSmemT<D>::stage + st * TcSmemT<D>::kStageBytes + TcSmemT<D>::NH * kHalf + c * kHalf;
 }
 
 // Byte offset of bf16 element (row, k) of a K-major 128-byte-swizzled tile whose
@@ -113,15 +125,17 @@ __device__ __forceinline__ uint32_t sw_elem(int row, int k, int block_bytes) {
 // 32 consecutive fp32 TMEM columns / 16 of them, this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) { tc::ld_32cols(taddr, v); }
 
-template <int G>
+template <int G, int D>
 __global__ void __launch_bounds__(192, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
     constexpr int HQ = kHeads * G;                 // query heads (MMA N)
+    using L = TcSmemT<D>;
+    constexpr int kStages = L::kStages;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TcSmem::bars);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     uint64_t* s_full = bars + 2 * kStages;
@@ -133,11 +147,11 @@ __global__ void __launch_bounds__(192, 1)
     // the four softmax warps meet here each tile (bounded waits, so a warp that stops
     // on a timed-out wait cannot leave the others blocked)
     uint64_t* grp = q_free + 2;
-    TcMeta* meta = reinterpret_cast<TcMeta*>(smem + TcSmem::meta);
-    float* alpha_buf = reinterpret_cast<float*>(smem + TcSmem::alpha);
-    float* l_buf = reinterpret_cast<float*>(smem + TcSmem::lbuf);
-    float* m_buf = reinterpret_cast<float*>(smem + TcSmem::mbuf);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::tmem_slot);
+    TcMeta* meta = reinterpret_cast<TcMeta*>(smem + L::meta);
+    float* alpha_buf = reinterpret_cast<float*>(smem + L::alpha);
+    float* l_buf = reinterpret_cast<float*>(smem + L::lbuf);
+    float* m_buf = reinterpret_cast<float*>(smem + L::mbuf);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -167,7 +181,11 @@ __global__ void __launch_bounds__(192, 1)
     }
     // P^T is block-diagonal: zero both buffers once; only diagonal entries are rewritten.
     for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(smem + TcSmem::pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(smem + L::pbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (D == 64) {   // the zero half standing for V^T rows 64..127
+        for (int i = threadIdx.x; i < kHalf / 16; i += blockDim.x)
+            reinterpret_cast<uint4*>(smem + L::zero)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -217,7 +235,7 @@ __global__ void __launch_bounds__(192, 1)
                 const int nvalid = min(kPosT, s1 - p0);
                 const int blk = __ldg(p.block_tables + (int64_t)b * p.M + p0 / p.P);
                 const bool okb = (unsigned)blk < (unsigned)p.N;
-                const uint32_t bytes = (okb ? (uint32_t)kStageBytes : 0u) + (j == 0 ? 2u * HQ * 128u : 0u);
+                const uint32_t bytes = (okb ? (uint32_t)L::kStageBytes : 0u) + (j == 0 ? 2u * HQ * (uint32_t)D : 0u);
                 if (lane == 0) {
                     if (!okb) report(p.dev_status, WF_DEV_BAD_BLOCK);
                     TcMeta m;
@@ -228,13 +246,14 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 __syncwarp();
                 const int slot = blk * p.P + p0 % p.P;
-                if (okb && lane < 4) {
-                    const CUtensorMap* tm = lane < 2 ? &tm_k : &tm_v;
-                    unsigned char* dst = lane < 2 ? stage_k(smem, st, lane & 1) : stage_v(smem, st, lane & 1);
-                    tma_load_3d(dst, tm, (lane & 1) * 64, slot, 0, &full[st], pol);
+                if (okb && lane < 2 * L::NH) {   // one 16 KB box per lane: K halves, then V halves
+                    const bool isv = lane >= L::NH;
+                    const int c = lane % L::NH;
+                    unsigned char* dst = isv ? stage_v<D>(smem, st, c) : stage_k<D>(smem, st, c);
+                    tma_load_3d(dst, isv ? &tm_v : &tm_k, c * 64, slot, 0, &full[st], pol);
                 }
-                if (j == 0 && (lane == 4 || lane == 5)) {
-                    tma_load_2d(smem + TcSmem::qbuf + qb * kQBytes + (lane - 4) * kQHalf, &tm_q, (lane - 4) * 64,
+                if (j == 0 && lane >= 4 && lane < 4 + L::NH) {
+                    tma_load_2d(smem + L::qbuf + qb * L::kQBytes + (lane - 4) * kQHalf, &tm_q, (lane - 4) * 64,
                                 b * p.H_q, &full[st]);
                 }
             }
@@ -255,15 +274,17 @@ __global__ void __launch_bounds__(192, 1)
         // ============================ MMA issuer ================================
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16_f32(kRows, HQ < 16 ? 16 : HQ, 0, 0);
-            constexpr uint32_t idO = tc::idesc_bf16_f32(kD, HQ < 16 ? 16 : HQ, 1, 0);
+            constexpr uint32_t idO = tc::idesc_bf16_f32(kRows, HQ < 16 ? 16 : HQ, 1, 0);
             auto issue_pv = [&](int u) {
                 const int su = u % kStages, ub = u & 1;
                 tc::fence_after_sync();
-                const uint32_t vbase = smem_u32(stage_v(smem, su, 0));
-                const uint32_t pb = smem_u32(smem + TcSmem::pbuf + ub * kPBytes);
+                const uint32_t vbase = smem_u32(stage_v<D>(smem, su, 0));
+                const uint32_t pb = smem_u32(smem + L::pbuf + ub * kPBytes);
+                // V^T rows 64..127: the tile's second half (D = 128) or the zero half (D = 64)
+                const uint32_t lbo = D == 128 ? (uint32_t)kHalf : smem_u32(smem + L::zero) - vbase;
 #pragma unroll
                 for (int kk = 0; kk < kRows / 16; ++kk) {
-                    const uint64_t ad = tc::sdesc_sw128(vbase + kk * 2048, kHalf, 1024);
+                    const uint64_t ad = tc::sdesc_sw128(vbase + kk * 2048, lbo, 1024);
                     const uint64_t bd = tc::sdesc_sw128(pb + (kk >> 2) * kPHalf + (kk & 3) * 32, 16, 1024);
                     tc::mma_f16(tmem + 64 + ub * 32, ad, bd, idO, kk > 0 ? 1u : 0u);
                 }
@@ -295,10 +316,10 @@ __global__ void __launch_bounds__(192, 1)
                         } else if (tq < 2 || mbar_test(&s_free[tq & 1], ((tq >> 1) - 1) & 1)) {
                             const int sb = tq & 1;
                             tc::fence_after_sync();
-                            const uint32_t kbase = smem_u32(stage_k(smem, st, 0));
-                            const uint32_t qbase = smem_u32(smem + TcSmem::qbuf + (m.item & 1) * kQBytes);
+                            const uint32_t kbase = smem_u32(stage_k<D>(smem, st, 0));
+                            const uint32_t qbase = smem_u32(smem + L::qbuf + (m.item & 1) * L::kQBytes);
 #pragma unroll
-                            for (int kk = 0; kk < kD / 16; ++kk) {
+                            for (int kk = 0; kk < D / 16; ++kk) {
                                 const uint64_t ad = tc::sdesc_sw128(kbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
                                 const uint64_t bd = tc::sdesc_sw128(qbase + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
                                 tc::mma_f16(tmem + sb * 32, ad, bd, idS, kk > 0 ? 1u : 0u);
@@ -361,17 +382,21 @@ __global__ void __launch_bounds__(192, 1)
                 acc[c + 3] = acc[c + 3] * a4.w + o[c + 3];
             }
             if (m.last) {
-                const float* L = l_buf + (m.item % 3) * kNq;
+                const float* Lsum = l_buf + (m.item % 3) * kNq;
                 const float* Mx = m_buf + (m.item % 3) * kNq;
                 if (m.nsplit == 1) {
-                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (int64_t)m.b * p.H_q * kD + i;
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (int64_t)m.b * p.H_q * D + i;
+                    if (i < D) {
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c) dst[c * kD] = __float2bfloat16_rn(acc[c] / L[c]);
+                        for (int c = 0; c < HQ; ++c) dst[c * D] = __float2bfloat16_rn(acc[c] / Lsum[c]);
+                    }
                 } else {
                     const int64_t base = ((int64_t)m.b * p.max_splits + m.split) * p.H_q;
+                    if (i < D) {
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c) p.ws_o[(base + c) * kD + i] = acc[c];
-                    if (i < HQ) p.ws_ml[base + i] = make_float2(Mx[i], L[i]);
+                        for (int c = 0; c < HQ; ++c) p.ws_o[(base + c) * D + i] = acc[c];
+                    }
+                    if (i < HQ) p.ws_ml[base + i] = make_float2(Mx[i], Lsum[i]);
                 }
             }
         };
@@ -409,7 +434,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             const bool live = pos < m.nvalid;
             float al[G];
-            unsigned char* pb = smem + TcSmem::pbuf + sb * kPBytes;
+            unsigned char* pb = smem + L::pbuf + sb * kPBytes;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float raw = upper ? sv[G + g] : sv[g];
@@ -443,8 +468,8 @@ __global__ void __launch_bounds__(192, 1)
             if (!live) {
                 // rows past the sequence end: zero V so their 0-weights cannot meet NaN/Inf
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint4* row = reinterpret_cast<uint4*>(stage_v(smem, st, c) + (i >> 3) * 1024 + (i & 7) * 128);
+                for (int c = 0; c < L::NH; ++c) {
+                    uint4* row = reinterpret_cast<uint4*>(stage_v<D>(smem, st, c) + (i >> 3) * 1024 + (i & 7) * 128);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -484,7 +509,8 @@ __global__ void decode_queue_reset_kernel(uint32_t* queue) {
 
 bool decode_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
     const int G = pool.num_kv_heads > 0 ? num_q_heads / pool.num_kv_heads : 0;
-    return pool.dtype == WF_DTYPE_BF16 && pool.head_dim == kD && pool.block_size % kPosT == 0 &&
+    return pool.dtype == WF_DTYPE_BF16 && (pool.head_dim == 64 || pool.head_dim == 128) &&
+           pool.block_size % kPosT == 0 &&
            pool.num_kv_heads == kHeads && num_q_heads % pool.num_kv_heads == 0 && (G == 2 || G == 4);
 }
 
@@ -497,12 +523,13 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
                                    float2* ws_ml, int32_t max_splits, uint32_t* queue, uint32_t* dev_status,
                                    cudaStream_t stream) {
     const int G = num_q_heads / pool.num_kv_heads;
+    const int D = pool.head_dim;
     CUtensorMap tm_k, tm_v, tm_q;
     const uint64_t slots = (uint64_t)pool.num_blocks * pool.block_size;
     {
         // (d, slot, head): one box = 16 slots x 8 heads x 64 d, head-major in shared memory
-        const uint64_t dims[3] = {(uint64_t)kD, slots, (uint64_t)kHeads};
-        const uint64_t strides[2] = {(uint64_t)kHeads * kD * 2, (uint64_t)kD * 2};
+        const uint64_t dims[3] = {(uint64_t)D, slots, (uint64_t)kHeads};
+        const uint64_t strides[2] = {(uint64_t)kHeads * D * 2, (uint64_t)D * 2};
         const uint32_t box[3] = {64, (uint32_t)kPosT, (uint32_t)kHeads};
         cudaError_t e = encode_tiled_bf16(&tm_k, const_cast<void*>(k_pool), 3, dims, strides, box);
         if (e != cudaSuccess) return e;
@@ -510,8 +537,8 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
         if (e != cudaSuccess) return e;
     }
     {
-        const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)B * num_q_heads};
-        const uint64_t strides[1] = {(uint64_t)kD * 2};
+        const uint64_t dims[2] = {(uint64_t)D, (uint64_t)B * num_q_heads};
+        const uint64_t strides[1] = {(uint64_t)D * 2};
         const uint32_t box[2] = {64, (uint32_t)num_q_heads};
         cudaError_t e = encode_tiled_bf16(&tm_q, const_cast<void*>(q), 2, dims, strides, box);
         if (e != cudaSuccess) return e;
@@ -534,13 +561,15 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
     p.P = pool.block_size;
     p.max_splits = max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const int smem = TcSmem::total + 1024;
+    const int smem = (D == 64 ? TcSmemT<64>::total : TcSmemT<128>::total) + 1024;
     const int64_t items = (int64_t)B * max_splits;
     const int grid = (int)(items < num_sms() ? items : num_sms());
     decode_queue_reset_kernel<<<1, 32, 0, stream>>>(queue);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const void* kern = G == 4 ? (const void*)paged_decode_tc_kernel<4> : (const void*)paged_decode_tc_kernel<2>;
+    const void* kern = D == 64 ? (G == 4 ? (const void*)paged_decode_tc_kernel<4, 64> : (const void*)paged_decode_tc_kernel<2, 64>)
+                               : (G == 4 ? (const void*)paged_decode_tc_kernel<4, 128>
+                                         : (const void*)paged_decode_tc_kernel<2, 128>);
     err = allow_dynamic_smem(kern, smem);
     if (err != cudaSuccess) return err;
     // a programmatic dependent of the reset: its set-up overlaps, its producer waits
@@ -554,8 +583,12 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (G == 4) return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<4>, tm_k, tm_v, tm_q, p);
-    return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<2>, tm_k, tm_v, tm_q, p);
+    if (D == 64) {
+        if (G == 4) return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<4, 64>, tm_k, tm_v, tm_q, p);
+        return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<2, 64>, tm_k, tm_v, tm_q, p);
+    }
+    if (G == 4) return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<4, 128>, tm_k, tm_v, tm_q, p);
+    return cudaLaunchKernelEx(&cfg, paged_decode_tc_kernel<2, 128>, tm_k, tm_v, tm_q, p);
 }
 
 }  // namespace wf

@@ -37,6 +37,10 @@ CASES = {
     "mha_f32_D128": lambda: W.custom_layout(4, 4, 128, 16, W.F32, [1000, 31], seed=6),
     "gqa4_D128_ragged": lambda: W.custom_layout(32, 8, 128, 16, W.BF16,
                                                 [1, 15, 16, 17, 127, 128, 129, 255, 256, 2049], seed=7),
+    # tensor-core decode at D = 64 (P.V over a zero upper half of V^T)
+    "gqa4_D64_ragged": lambda: W.custom_layout(32, 8, 64, 16, W.BF16,
+                                               [1, 15, 16, 17, 127, 128, 129, 255, 256, 2049], seed=14),
+    "gqa2_D64_P32_long": lambda: W.custom_layout(16, 8, 64, 32, W.BF16, [4000, 1, 300, 64, 33], seed=15),
 }
 
 
