@@ -20,7 +20,10 @@
 //   warps 8-10  producers: TMA loads of the two Q tiles (3D box d x head x token) and,
 //               tile by tile, of 128 keys of K and V gathered 16-key block by block
 //               through the block table (one box per lane, 128-byte swizzle) into a
-//               ring of K and V slots.
+//               ring of K and V slots.  The producer of a CTA's last V tile, when
+//               that tile runs past the CTA's last key, zeroes the rows past it (their
+//               weights are 0, but 0 * NaN is NaN in P.V) and releases the tile to
+//               P.V through its own barrier, off the softmax's path.
 //   warp 11     MMA issuer, event loop over both query tiles: S_t(j) = Q_t K_j^T
 //               (M=128, N=128 keys, K=D) into TMEM, O_t += P_t(j) V_j (M=128, N=D,
 //               K=128 keys, P from TMEM, V MN-major from shared memory); commits hand
@@ -81,8 +84,8 @@ struct PfLayout {
     static constexpr int tbl = kv + NSLOT * SLOT;
     static constexpr int bars = tbl + TBL * 4;
     // q_full, slot_full[NSLOT], slot_empty[NSLOT], then per query tile: s_full,
-    // p_full, pv_done
-    static constexpr int nbars = 1 + 2 * NSLOT + QT * 3;
+    // p_full, pv_done, then v_fixed
+    static constexpr int nbars = 1 + 2 * NSLOT + QT * 3 + 1;
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
     // TMEM: S of query tile t in columns [128 t, 128 t + 128) -- its softmax weights
@@ -139,6 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto s_full = [&](int t) { return tb + t * 3; };
     auto p_full = [&](int t) { return tb + t * 3 + 1; };
     auto pv_done = [&](int t) { return tb + t * 3 + 2; };
+    // the last V tile of a CTA whose last key tile is partial, once its rows past kend
+    // are zero
+    uint64_t* v_fixed = tb + 3 * L::QT;
+    const bool partial = kend % PN != 0;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
     int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::tbl);
     // load unit u (K(j): u = 2j, V(j): u = 2j + 1)
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(p_full(t), 4);
             mbar_init(pv_done(t), 1);
         }
+        mbar_init(v_fixed, 1);
         fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -211,6 +219,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 okb = (unsigned)blk < (unsigned)p.N;
                 if (!okb && isv == 0) report(p.dev_status, WF_DEV_BAD_BLOCK);
             }
+            if (isv && partial && j == ntiles - 1) {
+                // rows of 16-key blocks past the CTA's end are not loaded: zero them now
+                for (int rr = nbox * 16 + lane; rr < PN; rr += 32) {
+#pragma unroll
+                    for (int cb = 0; cb < L::NC; ++cb) {
+                        uint4* row = reinterpret_cast<uint4*>(unit_slot(u) + (rr >> 3) * L::ATOM + cb * L::HALF_OFF +
+                                                              (rr & 7) * 128);
+#pragma unroll
+                        for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
             const unsigned okm = __ballot_sync(0xffffffffu, okb);
             if (lane == 0) mbar_arrive_expect_tx(&slot_full[sl], (uint32_t)__popc(okm) * (uint32_t)L::BOX);
             __syncwarp();
@@ -222,6 +242,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     tma_load_3d_nohint(dst, isv ? &tm_v : &tm_k, 0, slot, h, &slot_full[sl]);
                 }
+            }
+            if (isv && partial && j == ntiles - 1) {
+                // keys past the CTA's end were not loaded (or hold whatever the pool has
+                // there): their P is 0, but 0 * NaN is NaN in P.V, so their V rows are
+                // zeroed once the tile has landed, before P.V may read it
+                if (!mbar_wait(&slot_full[sl], (uint32_t)(u / L::NSLOT) & 1u)) {
+                    if (lane == 0) report(p.dev_status, WF_DEV_TIMEOUT);
+                    break;
+                }
+                for (int rr = kend - k0 + lane; rr < nbox * 16; rr += 32) {   // the last block's tail
+#pragma unroll
+                    for (int cb = 0; cb < L::NC; ++cb) {
+                        uint4* row = reinterpret_cast<uint4*>(unit_slot(u) + (rr >> 3) * L::ATOM + cb * L::HALF_OFF +
+                                                              (rr & 7) * 128);
+#pragma unroll
+                        for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_fixed);
             }
         }
     } else if (warp == kMma) {
@@ -256,8 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = sp[t];
                 if (u < sq[t]) {
                     const int vu = 2 * u + 1;
+                    const bool vlast = partial && u == ntiles - 1;
                     const bool rdy = mbar_test(p_full(t), u & 1) &&
-                                     mbar_test(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1);
+                                     (vlast ? mbar_test(v_fixed, 0)
+                                            : mbar_test(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1));
                     if (__shfl_sync(0xffffffffu, (int)rdy, 0)) {
                         tc::fence_after_sync();
                         const uint32_t dO = tmem + L::OCOL + t * D;
@@ -429,23 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
             const float2 pst = __fadd2_rn(ps01, ps23);
             l_run += pst.x + pst.y;
-            if (k0 + PN > kend) {
-                // keys past the CTA's end were not loaded (or are stale): zero their V
-                // rows once V_j has landed.  Thread r owns key r; when both groups take
-                // part in this last tile they write the same zeros.
-                const int vu = 2 * j + 1;
-                if (!mbar_wait(&slot_full[vu % L::NSLOT], (vu / L::NSLOT) & 1)) report(p.dev_status, WF_DEV_TIMEOUT);
-                if (k0 + r >= kend) {
-#pragma unroll
-                    for (int cb = 0; cb < L::NC; ++cb) {
-                        uint4* row = reinterpret_cast<uint4*>(unit_slot(vu) + (r >> 3) * L::ATOM +
-                                                              cb * L::HALF_OFF + (r & 7) * 128);
-#pragma unroll
-                        for (int qq = 0; qq < 8; ++qq) row[qq] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-                tc::fence_proxy_async_smem();
-            }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(t));
