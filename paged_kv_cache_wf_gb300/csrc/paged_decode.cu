@@ -10,8 +10,10 @@
 //   * Work item = (sequence b, split j, group of HC <= 8 KV heads).  A split is a
 //     fixed span of positions that depends only on the pool geometry, so a
 //     sequence's result is the same whatever else is in the batch.
-//   * Persistent CTAs, one per SM.  CTA c takes items c, c + grid, ... and its
-//     producer warp streams their K and V rows, tile by tile (T positions), from
+//   * Persistent CTAs, one per SM.  CTA c takes items c, c + grid, ... (its
+//     producer maps an item to its sequence by a warp-parallel walk over 32
+//     sequence lengths per load round) and streams their K and V rows, tile by
+//     tile (T positions), from
 //     HBM into a ring of shared-memory stages with the bulk-copy (TMA) engine,
 //     without a pipeline restart between items.  Completion is an mbarrier
 //     transaction count; each stage also carries the tile's item description.
@@ -239,28 +241,19 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, 1) paged_decode_kernel(
         const int64_t pool_row = (int64_t)p.H_kv * D * EB;  // bytes of one pool slot
         const bool whole_rows = (p.HC == p.H_kv);           // slots contiguous across positions
         int t = 0;
-        int b = 0, len_b = 0, nsp_b = -1;
+        int b = 0, len_b = 0, nsp_b = 0;
         int64_t cum = 0;  // splits of sequences before b
         bool ok = true;
+        // the item -> sequence map walks 32 sequence lengths per load round (a CTA's
+        // items only move forward)
+        const int64_t cap = min((int64_t)p.max_seq_len, (int64_t)p.M * p.P);
+        ItemWalk walk;
+        item_walk_load(walk, p.seq_lens, p.B, p.split_span, cap, p.dev_status, lane);
         for (int64_t item = blockIdx.x; ok; item += gridDim.x) {
             const int64_t u = item / p.HG;
             const int hg = (int)(item % p.HG);
-            while (b < p.B) {
-                if (nsp_b < 0) {
-                    len_b = __ldg(p.seq_lens + b);
-                    if (len_ok(len_b, p)) {
-                        nsp_b = (len_b + p.split_span - 1) / p.split_span;
-                    } else {
-                        nsp_b = 0;
-                        if (lane == 0) report(p.dev_status, WF_DEV_BAD_SEQLEN);
-                    }
-                }
-                if (u < cum + nsp_b) break;
-                cum += nsp_b;
-                ++b;
-                nsp_b = -1;
-            }
-            if (b >= p.B) break;
+            if (!item_walk_find(walk, u, p.seq_lens, p.B, p.split_span, cap, p.dev_status, lane, b, len_b, nsp_b, cum))
+                break;
             const int split = (int)(u - cum);
             const int s0 = split * p.split_span;
             const int s1 = min(len_b, s0 + p.split_span);
