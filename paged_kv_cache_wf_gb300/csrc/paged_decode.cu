@@ -10,7 +10,9 @@
 //   * Work item = (sequence b, split j, group of HC <= 8 KV heads).  A split is a
 //     fixed span of positions that depends only on the pool geometry, so a
 //     sequence's result is the same whatever else is in the batch.
-//   * Persistent CTAs, one per SM.  CTA c takes items c, c + grid, ... (its
+//   * Persistent CTAs, one per SM (two per SM, with half the ring stages each, for
+//     group sizes up to 2, whose per-tile chain is short and latency-bound: two
+//     items in flight per SM).  CTA c takes items c, c + grid, ... (its
 //     producer maps an item to its sequence by a warp-parallel walk over 32
 //     sequence lengths per load round) and streams their K and V rows, tile by
 //     tile (T positions), from
@@ -202,8 +204,8 @@ __device__ __forceinline__ void load_v(const unsigned char* src, bool live, floa
     }
 }
 
-template <typename E, int D, int GMAX>
-__global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, 1) paged_decode_kernel(const DecodeParams p) {
+template <typename E, int D, int GMAX, int MINB>
+__global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kernel(const DecodeParams p) {
     using S = Shape<E, D, GMAX>;
     constexpr int T = S::T;
     constexpr int EB = S::EB;
@@ -621,9 +623,9 @@ int smem_bytes_for(int hc, int stages) {
            2 * hc * GMAX * S::T * 4 + hc * 8;
 }
 
-template <typename E, int D, int GMAX>
+template <typename E, int D, int GMAX, int MINB = 1>
 int pick_stages(int hc) {
-    constexpr int kBudget = 216 * 1024;
+    constexpr int kBudget = MINB == 1 ? 216 * 1024 : 108 * 1024;
     int st = 8;
     while (st > 2 && smem_bytes_for<E, D, GMAX>(hc, st) > kBudget) --st;
     return st;
@@ -631,13 +633,15 @@ int pick_stages(int hc) {
 
 template <typename E, int D, int GMAX>
 cudaError_t launch_typed(DecodeParams& p, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<E, D, GMAX>;
-    p.stages = pick_stages<E, D, GMAX>(p.HC);
+    // small group sizes run two CTAs per SM (half the stages each)
+    constexpr int MINB = GMAX <= 2 ? 2 : 1;
+    auto kern = paged_decode_kernel<E, D, GMAX, MINB>;
+    p.stages = pick_stages<E, D, GMAX, MINB>(p.HC);
     const int smem = smem_bytes_for<E, D, GMAX>(p.HC, p.stages);
     cudaError_t err = allow_dynamic_smem((const void*)kern, smem);
     if (err != cudaSuccess) return err;
     const int64_t items = (int64_t)p.B * p.max_splits * p.HG;
-    const int grid = (int)(items < num_sms() ? items : num_sms());
+    const int grid = (int)(items < MINB * num_sms() ? items : MINB * num_sms());
     kern<<<grid, (2 * p.HC + 1) * 32, smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
