@@ -671,9 +671,10 @@ bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeomet
             hc = c;
             break;
         }
-    // the tensor-core kernels (bf16, and every fp8 pool) have their own item span
-    g->split_span = decode_tc_supported(pool, num_q_heads) || pool.dtype == WF_DTYPE_FP8_E4M3 ? decode_tc_span()
-                                                                                              : kSpan;
+    // the tensor-core kernels (bf16, and every fp8 pool) have their own item spans
+    g->split_span = pool.dtype == WF_DTYPE_FP8_E4M3           ? decode_tc_fp8_span()
+                    : decode_tc_supported(pool, num_q_heads) ? decode_tc_span()
+                                                             : kSpan;
     g->tile = G > 4 ? 8 : 16;
     g->stages = 0;  // chosen per kernel instance at launch
     g->consumer_warps = 2 * hc;

@@ -56,7 +56,10 @@ namespace {
 constexpr int kRows = 128;       // MMA M: 8 heads x 16 positions (and D = 128 for P.V)
 constexpr int kHeads = 8;        // KV heads per tile
 constexpr int kPosT = 16;        // positions per tile
-constexpr int kSpanTc = 128;     // positions per item (split)
+// positions per item (split): 256 one-byte positions make an item the size of the
+// bf16 kernel's (512 KB over 8 KV heads); half as many partials to combine as with
+// 128 (measured 184 -> 176 us a call at the Llama-3-8B batch)
+constexpr int kSpanTc = 256;
 constexpr int kD = 128;
 constexpr int kNq = 32;          // max H_q handled (MMA N)
 constexpr int kStages = 5;
@@ -571,6 +574,8 @@ size_t decode_fp8_prep_bytes(int32_t B, int32_t num_q_heads) {
     const int64_t rows = (int64_t)B * num_q_heads;
     return (size_t)(2 * rows * 128 + rows * 4 + 256);
 }
+
+int decode_tc_fp8_span() { return kSpanTc; }
 
 bool decode_tc_fp8_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
     const int G = pool.num_kv_heads > 0 ? num_q_heads / pool.num_kv_heads : 0;

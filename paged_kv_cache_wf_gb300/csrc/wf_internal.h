@@ -71,6 +71,7 @@ cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool,
 // Tensor-core decode over fp8 e4m3 pools (H_kv = 8, D = 128, P % 16 == 0,
 // G in {2, 4}; bf16 q and outputs); same partials as the bf16 kernel.
 bool decode_tc_fp8_supported(const wf_pool_desc& pool, int32_t num_q_heads);
+int decode_tc_fp8_span();   // positions per work item of the fp8 kernel
 cudaError_t launch_paged_decode_tc_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                                        const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
