@@ -209,13 +209,13 @@ class DecodeWorkload:
         self.launches_per_layer = (3 if tc else 2) + (1 if -(-self.max_seq_len // self.split_span()) > 1 else 0)
 
     def split_span(self) -> int:
-        """Positions per decode work item: 256 for fp8 pools, 128 for the bf16
-        tensor-core kernel, 64 for the CUDA-core kernel."""
+        """Positions per decode work item: 256 for fp8 pools, 256 (D=128) or 128
+        (D=64) for the bf16 tensor-core kernel, 64 for the CUDA-core kernel."""
         g = self.lay.geom
         if self.kv == "fp8":
             return 256
         tc = g.H_kv == 8 and g.D in (64, 128) and g.P % 16 == 0 and g.H_q // g.H_kv in (2, 4)
-        return 128 if tc else 64
+        return (256 if g.D == 128 else 128) if tc else 64
 
     def _fp8_pools(self, seed):
         """e4m3 codes of the bf16 draws (torch's conversion after clamping to +-448;

@@ -4,7 +4,7 @@
 //
 // Same contract and split-K structure as the CUDA-core decode in
 // paged_decode.cu (ember, "The core idea"; tiny-vllm-py, "KV Cache"; weft,
-// "Shapes and symbols"): a work item is (sequence b, split of 128 positions), the
+// "Shapes and symbols"): a work item is (sequence b, split of tc_span(D) positions), the
 // split boundaries depend only on the pool geometry, and the items of a
 // multi-split sequence leave (m, l, o) partials for the combine kernel.
 //
@@ -51,7 +51,10 @@ namespace {
 constexpr int kRows = 128;       // MMA M: 8 heads x 16 positions (and D = 128 for P.V)
 constexpr int kHeads = 8;        // KV heads per tile
 constexpr int kPosT = 16;        // positions per tile
-constexpr int kSpanTc = 128;     // positions per item (split)
+// Positions per item (split): 256 at D = 128 (1 MB of K and V over the 8 KV heads;
+// half the partials of 128, measured 287 -> 275 us a call at the Llama-3-8B batch),
+// 128 at D = 64 (64 measured slower there).
+__host__ __device__ constexpr int tc_span(int D) { return D == 128 ? 256 : 128; }
 constexpr int kNq = 32;          // max H_q handled (MMA N, padded to a multiple of 16)
 constexpr int kEndTile = -1;
 constexpr int kHalf = kRows * 128;             // one 64-wide half of a K or V tile: 16 KB
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(192, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
     constexpr int HQ = kHeads * G;                 // query heads (MMA N)
+    constexpr int kSpan = tc_span(D);
     using L = TcSmemT<D>;
     constexpr int kStages = L::kStages;
     extern __shared__ unsigned char smem_raw[];
@@ -204,19 +208,19 @@ __global__ void __launch_bounds__(192, 1)
         bool ok = true;
         const int64_t cap = min((int64_t)p.max_seq_len, (int64_t)p.M * p.P);   // longest valid sequence
         ItemWalk walk;
-        item_walk_load(walk, p.seq_lens, p.B, kSpanTc, cap, p.dev_status, lane);
+        item_walk_load(walk, p.seq_lens, p.B, kSpan, cap, p.dev_status, lane);
         // Items come from a queue shared by all CTAs (one atomic increment per item,
         // claimed one item ahead so the round trip overlaps the current item's
         // copies).  Each CTA's claims increase, so its walk over the sequences only
         // moves forward.
         uint32_t claim = lane == 0 ? atomicAdd(p.queue, 1u) : 0u;
         for (int64_t item = __shfl_sync(0xffffffffu, claim, 0); ok; item = __shfl_sync(0xffffffffu, claim, 0)) {
-            if (!item_walk_find(walk, item, p.seq_lens, p.B, kSpanTc, cap, p.dev_status, lane, b, len, nsp, cum))
+            if (!item_walk_find(walk, item, p.seq_lens, p.B, kSpan, cap, p.dev_status, lane, b, len, nsp, cum))
                 break;
             claim = lane == 0 ? atomicAdd(p.queue, 1u) : 0u;
             const int split = (int)(item - cum);
-            const int s0 = split * kSpanTc;
-            const int s1 = min(len, s0 + kSpanTc);
+            const int s0 = split * kSpan;
+            const int s1 = min(len, s0 + kSpan);
             const int ntiles = (s1 - s0 + kPosT - 1) / kPosT;
             const int qb = k & 1;
             if (k >= 2 && !mbar_wait(&q_free[qb], ((k >> 1) - 1) & 1)) {
@@ -514,7 +518,7 @@ bool decode_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
            pool.num_kv_heads == kHeads && num_q_heads % pool.num_kv_heads == 0 && (G == 2 || G == 4);
 }
 
-int decode_tc_span() { return kSpanTc; }
+int decode_tc_span(int head_dim) { return tc_span(head_dim); }
 
 cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,

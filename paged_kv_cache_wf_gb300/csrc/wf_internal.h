@@ -60,7 +60,7 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
 // Tensor-core decode (bf16, D = 128, P % 16 == 0); writes outputs or split
 // partials exactly like the CUDA-core kernel, whose combine kernel finishes it.
 bool decode_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads);
-int decode_tc_span();
+int decode_tc_span(int head_dim);
 cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
                                    const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
