@@ -269,15 +269,25 @@ class DecodeWorkload:
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps * self.L)] if per_launch else None
         self._ev_done = []
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(self.stream)
-        for _ in range(steps):
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]   # step boundaries
+        marks[0].record(self.stream)
+        for i in range(steps):
             self.step(ev)
-        end.record(self.stream)
-        end.synchronize()
-        total_ms = start.elapsed_time(end)
+            marks[i + 1].record(self.stream)
+        marks[-1].synchronize()
+        total_ms = marks[0].elapsed_time(marks[-1])
+        self.step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
         launch_ms = [a.elapsed_time(b) for a, b in self._ev_done] if per_launch else []
         return total_ms, launch_ms
+
+
+def spread(xs):
+    """median, p10 and p90 of a list of timings (nearest-rank)."""
+    ys = sorted(xs)
+    if not ys:
+        return None
+    pick = lambda q: ys[min(len(ys) - 1, max(0, int(math.ceil(q * len(ys))) - 1))]
+    return {"median": statistics.median(ys), "p10": pick(0.10), "p90": pick(0.90), "n": len(ys)}
 
 
 def graph_timed(wl, steps: int) -> float:
@@ -794,12 +804,14 @@ def main():
                        "l2": "inputs larger than L2: each layer's pools are %.2f GB, read once per step"
                              % (2 * g.N * g.P * g.H_kv * g.D * kvb / 1e9),
                        "parallelism": f"replicas{world}"},
+            "step_ms_spread": spread(wl.step_ms),
             "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
             "pct_of_nominal_8tbs_step": 100.0 * step_bytes / (ms_per_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
             "roofline": {"kernel": "wf_paged_decode (split + combine)", "bound": "hbm", "achieved": achieved,
                          "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_source": peak_src,
                          "traffic": traffic, "algorithmic_bytes_per_launch": dbytes,
                          "avg_launch_us": avg_launch_s * 1e6,
+                         "launch_us_spread": spread([x * 1e3 for x in launch_ms]),
                          "pct_of_nominal_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS},
             "cpu_baseline": cpu,
             "e2e": e2e,
