@@ -23,7 +23,7 @@
 //     the V scale of each query head's KV head multiplies its output column.
 //
 // Work split, tiles and the (m, l, o) partials are those of the bf16 kernel: a work
-// item is (sequence b, split of 128 positions), a tile is one 16-position run of a
+// item is (sequence b, split of 256 positions), a tile is one 16-position run of a
 // block for all 8 KV heads -- 128 rows r = (head, position):
 //     S^T[128 rows x H_q] = K[128 rows x 128 d] . Q^T           (K-major A and B)
 //     O^T[128 d x H_q]    = V^T[128 d x 128 rows] . P^T          (V^T: MN-major A)

@@ -41,6 +41,11 @@ CASES = {
     "gqa4_D64_ragged": lambda: W.custom_layout(32, 8, 64, 16, W.BF16,
                                                [1, 15, 16, 17, 127, 128, 129, 255, 256, 2049], seed=14),
     "gqa2_D64_P32_long": lambda: W.custom_layout(16, 8, 64, 32, W.BF16, [4000, 1, 300, 64, 33], seed=15),
+    # around the work-item boundaries: 256 positions (tensor cores, D = 128) and 64
+    # positions (CUDA-core kernel)
+    "gqa4_D128_items256": lambda: W.custom_layout(32, 8, 128, 16, W.BF16,
+                                                  [255, 256, 257, 511, 512, 513, 768, 769], seed=16),
+    "mha12_items64": lambda: W.custom_layout(12, 12, 64, 16, W.BF16, [63, 64, 65, 128, 129, 193], seed=17),
 }
 
 

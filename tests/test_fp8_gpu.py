@@ -102,11 +102,13 @@ def test_fp8_scatter_flags_bad_slot_and_writes_the_rest():
 
 
 CASES = {
-    # Llama-3-8B heads (G=4), ragged lengths around the 16-position tile and 128-position split
+    # Llama-3-8B heads (G=4), ragged lengths around the 16-position tile
     "gqa4_ragged": lambda: W.custom_layout(32, 8, 128, 16, W.BF16,
                                            [1, 15, 16, 17, 127, 128, 129, 255, 256, 2049], seed=21),
     # G=2, larger blocks
     "gqa2_P32": lambda: W.custom_layout(16, 8, 128, 32, W.BF16, [1, 300, 1000, 64, 33], seed=22),
+    # around the 256-position work items
+    "gqa4_items256": lambda: W.custom_layout(32, 8, 128, 16, W.BF16, [255, 256, 257, 511, 512, 513, 1025], seed=24),
     # one long context in 64-slot blocks (many splits: combine path)
     "gqa4_long_P64": lambda: W.custom_layout(32, 8, 128, 64, W.BF16, [5000, 33, 128], seed=23),
 }
