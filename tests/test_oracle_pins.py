@@ -500,7 +500,7 @@ def _deq_per_head(torch, rows, scales):
 
 
 def test_fp8_per_head_scales_scatter_and_decode():
-    """One scale per KV head (the survey's per-head variant of the fp8 pool): head h's
+    """One scale per KV head (the per-head variant of the fp8 pool): head h's
     codes are torch's e4m3 cast of x * float32(1/scale_h), decode equals the
     contiguous brute force on the per-head dequantized values, equal per-head scales
     reproduce the per-tensor result exactly, and swapping two heads' scales breaks it."""
