@@ -323,7 +323,10 @@ def graph_timed(wl, steps: int) -> float:
 class E2EDecode:
     """The same step through host buffers: per layer, q / k_new / v_new come from
     pinned host memory and the attention output goes back to pinned host memory;
-    block tables, lengths and slots are uploaded once per step."""
+    block tables, lengths and slots are uploaded once per step.  The copies run on a
+    copy stream, as an engine would issue them: layer l + 1's inputs upload into the
+    other of two device input sets while layer l computes, and layer l's output is
+    read back as soon as its decode is done.  Every copy is inside the timed region."""
 
     def __init__(self, wl: DecodeWorkload):
         torch = wl.torch
@@ -333,36 +336,67 @@ class E2EDecode:
         self.h_bt = wl.bt.cpu().pin_memory()
         self.h_sl = wl.sl.cpu().pin_memory()
         self.h_slots = wl.slots.cpu().pin_memory()
-        self.d_vals = [torch.empty_like(t) for t in wl.vals[0]]
+        self.d_sets = [[torch.empty_like(t) for t in wl.vals[0]] for _ in range(2)]
         self.d_bt, self.d_sl, self.d_slots = (torch.empty_like(wl.bt), torch.empty_like(wl.sl),
                                               torch.empty_like(wl.slots))
+        self.cs = torch.cuda.Stream()          # host <-> device copies
         nb = lambda t: t.numel() * t.element_size()
         self.h2d = (sum(nb(t) for v in self.h_vals for t in v) + nb(self.h_bt) + nb(self.h_sl)
                     + nb(self.h_slots))
         self.d2h = sum(nb(t) for t in self.h_out)
 
-    def step(self):
-        wl = self.wl
-        self.d_bt.copy_(self.h_bt, non_blocking=True)
-        self.d_sl.copy_(self.h_sl, non_blocking=True)
-        self.d_slots.copy_(self.h_slots, non_blocking=True)
-        for l in range(wl.L):
-            q, k, v = self.d_vals
+    def step(self, after):
+        """One step; its copies start after event `after`.  Returns the event that
+        marks the last output copied back.  On the copy stream, layer l + 1's upload
+        is issued before layer l's read-back (which waits for layer l's decode), so it
+        overlaps layer l's kernels."""
+        torch, wl, cs, comp = self.wl.torch, self.wl, self.cs, self.wl.stream
+        cs.wait_event(after)
+        with torch.cuda.stream(cs):
+            self.d_bt.copy_(self.h_bt, non_blocking=True)
+            self.d_sl.copy_(self.h_sl, non_blocking=True)
+            self.d_slots.copy_(self.h_slots, non_blocking=True)
+        done = [None] * wl.L
+        ready = [None] * wl.L
+
+        def upload(l):
+            if l >= 2:
+                cs.wait_event(done[l - 2])       # the input set is free again
+            q, k, v = self.d_sets[l & 1]
             hq, hk, hv = self.h_vals[l]
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
+            with torch.cuda.stream(cs):
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+            ready[l] = torch.cuda.Event()
+            ready[l].record(cs)
+
+        upload(0)
+        for l in range(wl.L):
+            if l + 1 < wl.L:
+                upload(l + 1)
+            q, k, v = self.d_sets[l & 1]
+            comp.wait_event(ready[l])
             wl._scatter(l, k, v, self.d_slots)
             wl._decode(l, q, self.d_bt, self.d_sl, wl.outs[l])
-            self.h_out[l].copy_(wl.outs[l], non_blocking=True)
+            done[l] = torch.cuda.Event()
+            done[l].record(comp)
+            cs.wait_event(done[l])
+            with torch.cuda.stream(cs):
+                self.h_out[l].copy_(wl.outs[l], non_blocking=True)
+        last = torch.cuda.Event()
+        last.record(cs)
+        return last
 
     def timed(self, steps: int):
         torch = self.wl.torch
         s = self.wl.stream
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(s)
+        mark = start
         for _ in range(steps):
-            self.step()
+            mark = self.step(mark)
+        s.wait_event(mark)
         end.record(s)
         end.synchronize()
         return start.elapsed_time(end)
@@ -768,8 +802,10 @@ def main():
     e2e = None
     if not args.no_e2e:
         ee = E2EDecode(wl)
+        mark = torch.cuda.Event()
+        mark.record(wl.stream)
         for _ in range(3):
-            ee.step()
+            mark = ee.step(mark)
         torch.cuda.synchronize()
         if pg is not None:
             pg.barrier()
