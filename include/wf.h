@@ -162,11 +162,14 @@ size_t wf_paged_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t ma
  * Launches a split-K kernel and, when any sequence spans more than one split, a
  * combine kernel.  The split boundaries depend only on the pool geometry, so a
  * sequence's output does not depend on the rest of the batch.
- * fp8 e4m3 pools: q and out are bfloat16; K_p and V_p are k_scale * value and
- * v_scale * value of the stored codes.  Supported for H_kv = 8, D = 128, P a
- * multiple of 16, H_q / H_kv in {2, 4} and N*P <= 2^31 - 1 (WF_ERR_UNSUPPORTED
- * otherwise).  Both products run on the tensor cores in fp16 (every e4m3 value is
- * an fp16 value, q is rounded to fp16, the softmax weights are rounded to fp16).
+ * fp8 e4m3 pools: q and out are bfloat16; K_p and V_p are k_scale_h * value and
+ * v_scale_h * value of the stored codes (h the KV head; per-pool or per-head
+ * scales).  Every geometry of the bf16 path is supported.  For H_kv = 8, D = 128,
+ * P a multiple of 16, H_q / H_kv in {2, 4} and N*P <= 2^31 - 1 both products run
+ * on the tensor cores on the codes (e4m3 x e4m3 -> fp32): q is split into two e4m3
+ * parts whose sum is q exactly, and the softmax weights into two parts (about 8
+ * significant bits).  Other shapes run on the CUDA cores, which widen the codes to
+ * fp32 exactly and keep fp32 weights.
  */
 wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
                           const int32_t* block_tables, int32_t max_blocks_per_seq,

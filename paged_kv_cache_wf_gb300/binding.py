@@ -165,6 +165,9 @@ def pool_desc(k_pool, k_scale=1.0, v_scale=1.0) -> wf_pool_desc:
         raise TypeError(f"unsupported pool dtype {k_pool.dtype}")
     ks, karr = _scale_arg(k_scale)
     vs, varr = _scale_arg(v_scale)
+    for arr in (karr, varr):
+        if arr is not None and len(arr) != H_kv:
+            raise ValueError(f"per-head scales need one value per KV head ({H_kv}), got {len(arr)}")
     d = wf_pool_desc(N, P, H_kv, D, dt, ks, vs, karr, varr)
     d._keep = (karr, varr)   # the host arrays live as long as the descriptor
     return d

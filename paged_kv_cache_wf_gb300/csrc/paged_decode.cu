@@ -68,6 +68,20 @@ struct DecodeParams {
     int32_t max_splits;
     int32_t stages;
     float scale_log2;    // scale * log2(e)
+    // fp8 e4m3 pools: the scale of each KV head's K and V codes (a code c of head h
+    // stands for k_head[h] * value(c)); unused for fp32 and bf16 pools
+    float k_head[kMaxScaleHeads];
+    float v_head[kMaxScaleHeads];
+};
+
+// q and the outputs: the pool's type, except that fp8 pools take bf16 ones.
+template <typename E>
+struct QType {
+    using type = E;
+};
+template <>
+struct QType<FP8> {
+    using type = BF16;
 };
 
 // What the producer tells the consumers about the tile in a stage.
@@ -172,7 +186,20 @@ __device__ __forceinline__ int head_lane(int g) {
 
 template <typename E, int LB>
 __device__ __forceinline__ void load_widen(const unsigned char* src, float* f) {
-    if constexpr (LB == 16) {
+    if constexpr (E::kBytes == 1) {  // LB e4m3 codes
+        if constexpr (LB == 8) {
+            const uint2 u = ld_shared_v2(src);
+            const float2 a = e4m3x2_to_float2(u.x), b = e4m3x2_to_float2(u.x >> 16);
+            const float2 c = e4m3x2_to_float2(u.y), d = e4m3x2_to_float2(u.y >> 16);
+            f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+            f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+        } else {
+            static_assert(LB == 4, "fp8 K loads of 4 or 8 codes");
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+            const float2 a = e4m3x2_to_float2(u), b = e4m3x2_to_float2(u >> 16);
+            f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+        }
+    } else if constexpr (LB == 16) {
         widen_chunk<E>(ld_shared_v4(src), f);
     } else {  // 8 bytes of bf16
         const uint2 u = ld_shared_v2(src);
@@ -184,7 +211,15 @@ __device__ __forceinline__ void load_widen(const unsigned char* src, float* f) {
 // One lane's VPL dims of V at one position, as fp32 (0 when `live` is false).
 template <typename E, int VPL>
 __device__ __forceinline__ void load_v(const unsigned char* src, bool live, float* f) {
-    if constexpr (E::kBytes == 2) {
+    if constexpr (E::kBytes == 1) {  // e4m3 codes
+        if constexpr (VPL == 2) {
+            const float2 x = e4m3x2_to_float2(live ? (uint32_t)(*reinterpret_cast<const uint16_t*>(src)) : 0u);
+            f[0] = x.x;
+            f[1] = x.y;
+        } else {
+            f[0] = e4m3x2_to_float2(live ? (uint32_t)(*src) : 0u).x;
+        }
+    } else if constexpr (E::kBytes == 2) {
         if constexpr (VPL == 2) {
             const uint32_t u = live ? *reinterpret_cast<const uint32_t*>(src) : 0u;
             f[0] = __uint_as_float(u << 16);
@@ -332,6 +367,9 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kern
     const int off_r = reduced_offset<S::NV, S::DG>(lane);
     const int g_lane = off_r / S::NPL;  // query head of this lane's finished dots
 
+    using QE = typename QType<E>::type;                // q and output element type
+    constexpr int QB = S::EPL * QE::kBytes;            // bytes of q per K load chunk
+    constexpr bool kCodes = E::kBytes == 1;            // fp8 e4m3 pool
     float2 q2[GMAX][S::DPL / 2];
     float2 acc[GMAX][S::VPL];
     float m_run = -INFINITY, l_run = 0.f;
@@ -357,9 +395,9 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kern
                     float f[S::EPL];
                     if (g < G) {
                         const char* src = static_cast<const char*>(p.q) +
-                                          (((int64_t)mt.b * p.H_q + hq0 + g) * D + half * S::DH) * EB + c * S::LB;
-                        if constexpr (S::LB == 16) {
-                            widen_chunk<E>(*reinterpret_cast<const uint4*>(src), f);
+                                          (((int64_t)mt.b * p.H_q + hq0 + g) * D + half * S::DH) * QE::kBytes + c * QB;
+                        if constexpr (QB == 16) {
+                            widen_chunk<QE>(*reinterpret_cast<const uint4*>(src), f);
                         } else {
                             const uint2 u = *reinterpret_cast<const uint2*>(src);
                             const float2 a = bf16x2_to_float2(u.x), bb = bf16x2_to_float2(u.y);
@@ -369,10 +407,13 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kern
 #pragma unroll
                         for (int e = 0; e < S::EPL; ++e) f[e] = 0.f;
                     }
+                    // fp8: scores are formed from the code values, so the K scale of this
+                    // warp's KV head goes into q
+                    float qs = p.scale_log2;
+                    if constexpr (kCodes) qs = p.scale_log2 * p.k_head[mt.hg * p.HC + pair];
 #pragma unroll
                     for (int e = 0; e < S::EPL / 2; ++e)
-                        q2[g][k * S::EPL / 2 + e] =
-                            make_float2(f[2 * e] * p.scale_log2, f[2 * e + 1] * p.scale_log2);
+                        q2[g][k * S::EPL / 2 + e] = make_float2(f[2 * e] * qs, f[2 * e + 1] * qs);
                 }
             }
 #pragma unroll
@@ -502,12 +543,14 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kern
 #pragma unroll
                 for (int g = 0; g < GMAX; ++g) {
                     if (g < G) {
-                        const float inv = 1.f / Lh[g];
+                        float inv = 1.f / Lh[g];
+                        if constexpr (kCodes) inv *= p.v_head[mt.hg * p.HC + pair];   // the V scale
                         float o[S::VPL];
 #pragma unroll
                         for (int vv = 0; vv < S::VPL; ++vv) o[vv] = (acc[g][vv].x + acc[g][vv].y) * inv;
-                        char* dst = static_cast<char*>(p.out) + (((int64_t)mt.b * p.H_q + hq0 + g) * D + dcol) * EB;
-                        store_out<E, S::VPL>(dst, o);
+                        char* dst =
+                            static_cast<char*>(p.out) + (((int64_t)mt.b * p.H_q + hq0 + g) * D + dcol) * QE::kBytes;
+                        store_out<QE, S::VPL>(dst, o);
                     }
                 }
             } else {
@@ -516,8 +559,10 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kern
                 for (int g = 0; g < GMAX; ++g) {
                     if (g < G) {
                         float* dst = p.ws_o + (base + g) * D + dcol;
+                        float vsc = 1.f;
+                        if constexpr (kCodes) vsc = p.v_head[mt.hg * p.HC + pair];   // partials carry the V scale
 #pragma unroll
-                        for (int vv = 0; vv < S::VPL; ++vv) dst[vv] = acc[g][vv].x + acc[g][vv].y;
+                        for (int vv = 0; vv < S::VPL; ++vv) dst[vv] = (acc[g][vv].x + acc[g][vv].y) * vsc;
                         if (half == 0 && lane == 0) p.ws_ml[base + g] = make_float2(Mh[g], Lh[g]);
                     }
                 }
@@ -645,7 +690,7 @@ cudaError_t launch_typed(DecodeParams& p, cudaStream_t stream) {
     kern<<<grid, (2 * p.HC + 1) * 32, smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    return p.max_splits > 1 ? launch_combine<E, D>(p, stream) : cudaSuccess;
+    return p.max_splits > 1 ? launch_combine<typename QType<E>::type, D>(p, stream) : cudaSuccess;
 }
 
 template <typename E, int D>
@@ -660,6 +705,12 @@ cudaError_t launch_group(DecodeParams& p, int gmax, cudaStream_t stream) {
 
 }  // namespace
 
+// fp8 pools run the tensor-core kernel where it takes their shape, else this file's
+// CUDA-core kernel on the codes.
+static bool fp8_on_tensor_cores(const wf_pool_desc& pool, int32_t num_q_heads) {
+    return decode_tc_fp8_supported(pool, num_q_heads) && (int64_t)pool.num_blocks * pool.block_size <= INT32_MAX;
+}
+
 bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeometry* g) {
     if (pool.num_kv_heads < 1 || num_q_heads % pool.num_kv_heads != 0) return false;
     const int G = num_q_heads / pool.num_kv_heads;
@@ -672,7 +723,8 @@ bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeomet
             break;
         }
     // the tensor-core kernels (bf16, and every fp8 pool) have their own item spans
-    g->split_span = pool.dtype == WF_DTYPE_FP8_E4M3           ? decode_tc_fp8_span()
+    g->split_span = pool.dtype == WF_DTYPE_FP8_E4M3
+                        ? (fp8_on_tensor_cores(pool, num_q_heads) ? decode_tc_fp8_span() : kSpan)
                     : decode_tc_supported(pool, num_q_heads) ? decode_tc_span(pool.head_dim)
                                                              : kSpan;
     g->tile = G > 4 ? 8 : 16;
@@ -744,9 +796,17 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
         if (p.max_splits <= 1) return cudaSuccess;
         return pool.head_dim == 64 ? launch_combine<BF16, 64>(p, stream) : launch_combine<BF16, 128>(p, stream);
     }
+    if (pool.dtype == WF_DTYPE_FP8_E4M3 && !fp8_on_tensor_cores(pool, num_q_heads)) {
+        // other shapes: the CUDA-core kernel widens the codes; per-head scales by value
+        const HeadScales hs = head_scales(pool);
+        for (int h = 0; h < kMaxScaleHeads; ++h) {
+            p.k_head[h] = hs.k[h];
+            p.v_head[h] = hs.v[h];
+        }
+        return pool.head_dim == 64 ? launch_group<FP8, 64>(p, g.gmax, stream)
+                                   : launch_group<FP8, 128>(p, g.gmax, stream);
+    }
     if (pool.dtype == WF_DTYPE_FP8_E4M3) {
-        // e4m3 pools have only the tensor-core path; the entry point rejects other shapes
-        if (!decode_tc_fp8_supported(pool, num_q_heads) || slots > INT32_MAX) return cudaErrorInvalidValue;
         // the preparing grid zeroes the queue; its q parts follow the partials
         void* prep = static_cast<char*>(workspace) + (o_bytes + rows * 8 + 256 + 255) / 256 * 256;
         cudaError_t err = launch_paged_decode_tc_fp8(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,

@@ -174,10 +174,6 @@ wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const vo
     if (B < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 1) return WF_ERR_INVALID_ARG;
     if (num_q_heads % pool.num_kv_heads != 0) return WF_ERR_INVALID_ARG;
     if (num_q_heads / pool.num_kv_heads > 8) return WF_ERR_UNSUPPORTED;
-    if (pool.dtype == WF_DTYPE_FP8_E4M3 &&
-        (!wf::decode_tc_fp8_supported(pool, num_q_heads) ||
-         (int64_t)pool.num_blocks * pool.block_size > INT32_MAX))
-        return WF_ERR_UNSUPPORTED;
     if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool.block_size) return WF_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return WF_ERR_INVALID_ARG;
     if (B == 0) return WF_OK;

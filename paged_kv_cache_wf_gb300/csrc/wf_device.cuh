@@ -32,6 +32,19 @@ struct BF16 {
     static constexpr int kBytes = 2;
     static constexpr int kPerChunk = 8;
 };
+// fp8 e4m3 pool codes (q and outputs of such pools are bf16)
+struct FP8 {
+    static constexpr int kBytes = 1;
+    static constexpr int kPerChunk = 16;
+};
+
+// Two e4m3 codes (low 16 bits) -> two floats, exactly (every e4m3 value is an fp16
+// value), by the hardware conversion.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+    const __half2 h = r;
+    return __half22float2(h);
+}
 
 // bf16 is the upper half of an fp32: widening is a shift / mask.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {

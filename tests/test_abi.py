@@ -148,8 +148,9 @@ def _load_fresh(path):
 
 
 def test_fp8_pool_argument_checks(lib):
-    """fp8 e4m3 pools need finite positive scales; decode takes them only in the
-    shapes the tensor-core kernel handles; prefill does not take them."""
+    """fp8 e4m3 pools need finite positive scales; decode takes them in every
+    geometry the bf16 path takes (tensor cores or CUDA cores); prefill does not
+    take them."""
     sc = lib.wf_reshape_and_cache
     for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
         assert sc(FAKE, FAKE, FAKE, FAKE, FAKE, 0, _fp8(ks=ks, vs=vs), None, None) == wf.WF_ERR_INVALID_ARG
@@ -165,11 +166,13 @@ def test_fp8_pool_argument_checks(lib):
 
     assert dec(_fp8()) == wf.WF_OK                                    # G = 4: supported (B = 0: no-op)
     assert dec(_fp8(), Hq=16) == wf.WF_OK                             # G = 2
-    assert dec(_fp8(), Hq=8) == wf.WF_ERR_UNSUPPORTED                 # G = 1
-    assert dec(_fp8(), Hq=64) == wf.WF_ERR_UNSUPPORTED                # G = 8
-    assert dec(_fp8(D=64)) == wf.WF_ERR_UNSUPPORTED
-    assert dec(_fp8(H=4), Hq=16) == wf.WF_ERR_UNSUPPORTED
-    assert dec(_fp8(P=8)) == wf.WF_ERR_UNSUPPORTED
+    assert dec(_fp8(), Hq=8) == wf.WF_OK                              # G = 1 (CUDA cores)
+    assert dec(_fp8(), Hq=64) == wf.WF_OK                             # G = 8
+    assert dec(_fp8(D=64)) == wf.WF_OK
+    assert dec(_fp8(H=4), Hq=16) == wf.WF_OK
+    assert dec(_fp8(P=24)) == wf.WF_OK                              # P % 16 != 0
+    assert dec(_fp8(), Hq=72) == wf.WF_ERR_UNSUPPORTED                # G = 9, as for bf16
+    assert dec(_fp8(D=96)) == wf.WF_ERR_UNSUPPORTED                   # as for bf16
     assert dec(_fp8(ks=0.0)) == wf.WF_ERR_INVALID_ARG
 
     pf = lib.wf_paged_prefill

@@ -109,6 +109,10 @@ CASES = {
     "gqa2_P32": lambda: W.custom_layout(16, 8, 128, 32, W.BF16, [1, 300, 1000, 64, 33], seed=22),
     # around the 256-position work items
     "gqa4_items256": lambda: W.custom_layout(32, 8, 128, 16, W.BF16, [255, 256, 257, 511, 512, 513, 1025], seed=24),
+    # shapes the tensor-core kernel does not take: the CUDA-core kernel widens the codes
+    "core_mha12_D64": lambda: W.custom_layout(12, 12, 64, 16, W.BF16, [700, 1, 256, 63, 65], seed=25),
+    "core_gqa8_D128_P7": lambda: W.custom_layout(16, 2, 128, 7, W.BF16, [300, 1, 129, 128, 127], seed=26),
+    "core_gqa4_D64": lambda: W.custom_layout(32, 8, 64, 16, W.BF16, [1, 15, 257, 2049], seed=27),
     # one long context in 64-slot blocks (many splits: combine path)
     "gqa4_long_P64": lambda: W.custom_layout(32, 8, 128, 64, W.BF16, [5000, 33, 128], seed=23),
 }
@@ -256,8 +260,11 @@ def test_fp8_decode_flags_bad_seq_len():
 
 
 # one scale per KV head: spread over three octaves and not powers of two
-K_HEAD = [1 / 64 * (1.37 ** (h - 4)) for h in range(8)]
-V_HEAD = [1 / 96 * (0.71 ** (h - 3)) for h in range(8)]
+def _head_scales(H_kv):
+    return ([1 / 64 * (1.37 ** (h - 4)) for h in range(H_kv)], [1 / 96 * (0.71 ** (h - 3)) for h in range(H_kv)])
+
+
+K_HEAD, V_HEAD = _head_scales(8)
 
 
 def test_fp8_per_head_scatter_bit_exact():
@@ -279,7 +286,7 @@ def test_fp8_per_head_scatter_bit_exact():
     assert wf.wf_device_status_fetch(st) == 0
 
 
-@pytest.mark.parametrize("name", ["gqa4_ragged", "gqa2_P32"])
+@pytest.mark.parametrize("name", ["gqa4_ragged", "gqa2_P32", "core_mha12_D64", "core_gqa4_D64"])
 def test_fp8_per_head_decode_matches_oracle(name):
     torch = G.torch_mod()
     lay = CASES[name]()
@@ -287,16 +294,17 @@ def test_fp8_per_head_decode_matches_oracle(name):
     g = lay.geom
     scale = G.default_scale(g.D)
     st = G.dev_status()
-    (dk, dv), (hk, hv) = _pools_both(lay, vals, K_HEAD, V_HEAD, st)
+    kh, vh = _head_scales(g.H_kv)
+    (dk, dv), (hk, hv) = _pools_both(lay, vals, kh, vh, st)
     assert np.array_equal(dk.cpu().numpy(), hk) and np.array_equal(dv.cpu().numpy(), hv)
     q = G.to_dev(vals.q, W.BF16)
     out = torch.empty_like(q)
     ws = torch.empty(wf.wf_paged_decode_workspace_size(lay.B, g.H_q, lay.max_seq_len,
-                                                       wf.pool_desc(dk, K_HEAD, V_HEAD)),
+                                                       wf.pool_desc(dk, kh, vh)),
                      dtype=torch.uint8, device="cuda")
     wf.wf_paged_decode(out, q, dk, dv, torch.from_numpy(lay.block_tables).cuda(),
                        torch.from_numpy(lay.seq_lens).cuda(), lay.max_seq_len, scale, ws, st,
-                       k_scale=K_HEAD, v_scale=V_HEAD)
+                       k_scale=kh, v_scale=vh)
     assert wf.wf_device_status_fetch(st) == 0
-    ref = oracle.paged_decode_fp8(vals.q, hk, hv, lay.block_tables, lay.seq_lens, scale, K_HEAD, V_HEAD)
+    ref = oracle.paged_decode_fp8(vals.q, hk, hv, lay.block_tables, lay.seq_lens, scale, kh, vh)
     G.assert_close(G.from_dev(out, W.BF16), ref, W.BF16, f"fp8 per-head {name}")
