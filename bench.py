@@ -205,17 +205,21 @@ class DecodeWorkload:
         self.sp = self.stream.cuda_stream
         # scatter, the grid that zeroes the work queue (fp8: and prepares q), the
         # split kernel, and the combine when any sequence has more than one split
-        tc = g.H_kv == 8 and g.D in (64, 128) and g.P % 16 == 0 and g.H_q // g.H_kv in (2, 4)
-        self.launches_per_layer = (3 if tc else 2) + (1 if -(-self.max_seq_len // self.split_span()) > 1 else 0)
+        self.launches_per_layer = (3 if self.tensor_cores() else 2) + (
+            1 if -(-self.max_seq_len // self.split_span()) > 1 else 0)
+
+    def tensor_cores(self) -> bool:
+        """Whether the library runs this decode on its tensor-core kernel."""
+        g = self.lay.geom
+        shape = g.H_kv == 8 and g.P % 16 == 0 and g.H_q // g.H_kv in (2, 4)
+        return shape and (g.D == 128 if self.kv == "fp8" else g.D in (64, 128))
 
     def split_span(self) -> int:
-        """Positions per decode work item: 256 for fp8 pools, 256 (D=128) or 128
-        (D=64) for the bf16 tensor-core kernel, 64 for the CUDA-core kernel."""
-        g = self.lay.geom
-        if self.kv == "fp8":
-            return 256
-        tc = g.H_kv == 8 and g.D in (64, 128) and g.P % 16 == 0 and g.H_q // g.H_kv in (2, 4)
-        return (256 if g.D == 128 else 128) if tc else 64
+        """Positions per decode work item: 256 on the tensor cores for fp8 pools and
+        for bf16 at D=128, 128 for bf16 at D=64, 64 on the CUDA cores."""
+        if not self.tensor_cores():
+            return 64
+        return 256 if self.kv == "fp8" or self.lay.geom.D == 128 else 128
 
     def _fp8_pools(self, seed):
         """e4m3 codes of the bf16 draws (torch's conversion after clamping to +-448;
@@ -702,13 +706,13 @@ def oracle_time(sub, hk, hv, q, kn, vn, min_seconds: float, max_reps: int, fp8_s
 # main
 # ---------------------------------------------------------------------------
 def make_layout(args):
+    sfx = "_fp8kv" if args.kv == "fp8" else ""
     if args.workload == "llama8b":
-        sfx = "_fp8kv" if args.kv == "fp8" else ""
         return W.llama8b_decode(args.batch, seed=0), f"llama8b_decode_B{args.batch}{sfx}"
     if args.workload == "gpt2":
-        return W.gpt2_decode(0), "gpt2_decode_B32"
+        return W.gpt2_decode(0), f"gpt2_decode_B32{sfx}"
     if args.workload == "llama1b":
-        return W.llama1b_decode(0), "llama1b_decode_B64"
+        return W.llama1b_decode(0), f"llama1b_decode_B64{sfx}"
     raise SystemExit(f"unknown workload {args.workload}")
 
 
@@ -751,7 +755,7 @@ def main():
     ap.add_argument("--workload", default="llama8b", choices=["llama8b", "gpt2", "llama1b", "mixed", "cow"])
     ap.add_argument("--impl", default="wf", choices=["wf", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
-                    help="KV pool format of the decode workloads (fp8: e4m3 codes; Llama-3-8B shapes only)")
+                    help="KV pool format of the decode workloads (fp8: e4m3 codes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -787,8 +791,6 @@ def main():
         if pg is not None:
             pg.destroy_process_group()
         return
-    if args.kv == "fp8" and args.workload != "llama8b":
-        raise SystemExit("--kv fp8 runs the Llama-3-8B decode workload only")
     lay, wname = make_layout(args)
     g = lay.geom
     L = args.layers if args.layers > 0 else g.L
