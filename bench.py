@@ -53,6 +53,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(pg, x: float, device: str = "cuda") -> float:
+    """The largest of every rank's value (replicas are timed by their slowest rank);
+    x itself without a process group."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank processes units_per_rank in ms (the slowest
+    rank's time)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -817,12 +834,9 @@ def main():
     clk = clocks.stop()
     if wl.wf.wf_device_status_fetch(wl.status) != 0:
         raise SystemExit("device status flagged an error during the timed steps")
-    if pg is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, total_ms)
     ms_per_step = total_ms / args.steps
-    value = world * lay.B * L / (ms_per_step / 1e3)
+    value = job_rate(world, lay.B * L, ms_per_step)
 
     # ---- roofline of the decode call (split + combine kernels) -------------------
     peaks, peak_src = load_peaks()
@@ -837,14 +851,10 @@ def main():
     # ---- the same step as one replayed CUDA graph ---------------------------------------
     graph = None
     if not args.no_graph:
-        g_ms = graph_timed(wl, args.steps)
-        if pg is not None:
-            t = torch.tensor([g_ms], device="cuda")
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            g_ms = float(t.item())
+        g_ms = max_over_ranks(pg, graph_timed(wl, args.steps))
         if wl.wf.wf_device_status_fetch(wl.status) != 0:
             raise SystemExit("device status flagged an error during the graph replays")
-        graph = {"value": world * lay.B * L / (g_ms / 1e3), "unit": UNIT, "ms_per_step": g_ms,
+        graph = {"value": job_rate(world, lay.B * L, g_ms), "unit": UNIT, "ms_per_step": g_ms,
                  "note": "the step (scatter + decode for every layer) captured once as a CUDA graph and replayed"}
 
     # ---- end to end through host buffers --------------------------------------------
@@ -858,12 +868,8 @@ def main():
         torch.cuda.synchronize()
         if pg is not None:
             pg.barrier()
-        e_ms = ee.timed(args.steps) / args.steps
-        if pg is not None:
-            t = torch.tensor([e_ms], device="cuda")
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * lay.B * L / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+        e_ms = max_over_ranks(pg, ee.timed(args.steps) / args.steps)
+        e2e = {"value": job_rate(world, lay.B * L, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": ee.h2d, "d2h_bytes_per_step": ee.d2h}
         del ee
 
