@@ -887,13 +887,15 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8e4m3 KV, f16 MMA" if fp8 else "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": ("e4m3 (e4m3 x e4m3 MMA, fp32 accumulate)" if wl.tensor_cores()
+                                                     else "f32 (e4m3 codes widened to fp32)") if fp8 else "bf16", "data": "synthetic",
             "config": {"workload": wname, "B": lay.B, "layers": L, "model_layers": g.L, "H_q": g.H_q,
                        "H_kv": g.H_kv, "D": g.D, "P": g.P, "N_blocks_per_layer": g.N,
                        "kv_dtype": "fp8_e4m3" if fp8 else g.dtype,
                        "context_tokens": int(lay.seq_lens.sum()), "max_seq_len": lay.max_seq_len,
-                       "l2": "inputs larger than L2: each layer's pools are %.2f GB, read once per step"
-                             % (2 * g.N * g.P * g.H_kv * g.D * kvb / 1e9),
+                       "l2": "inputs larger than L2: each layer's pools (%.2f GB) are read once per step, "
+                             "and the step reads %.2f GB of pools between two reads of one layer's"
+                             % (2 * g.N * g.P * g.H_kv * g.D * kvb / 1e9, L * 2 * g.N * g.P * g.H_kv * g.D * kvb / 1e9),
                        "parallelism": f"replicas{world}"},
             "step_ms_spread": spread(wl.step_ms),
             "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
