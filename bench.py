@@ -635,7 +635,9 @@ def run_mixed(args, rank, world):
         "data": "synthetic",
         "config": {"workload": "mixed_llama8b", "prefill_requests": pf.B, "prefill_tokens": int(pf.q_lens.sum()),
                    "decode_sequences": dc.B, "layers": L, "model_layers": g.L, "H_q": g.H_q, "H_kv": g.H_kv,
-                   "D": g.D, "P": g.P},
+                   "D": g.D, "P": g.P,
+                   "l2": "inputs larger than L2: each layer has its own pools (%.2f GB), read once per step"
+                         % (2 * g.N * g.P * g.H_kv * g.D * W.elt_size(g.dtype) / 1e9)},
         "roofline": {"kernel": "wf_paged_prefill", "bound": "tensor", "achieved": tflops, "peak": peak_t,
                      "unit": "TFLOP/s", "frac": tflops / peak_t, "peak_source": src,
                      "algorithmic_flops_per_launch": flops, "avg_launch_us": pre_s * 1e6,
