@@ -202,7 +202,8 @@ wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const v
 
 /*
  * Size of the fixed device array wf_paged_decode_static_scratch uses as its
- * workspace (32 MiB).  Every GPU that loads libwf holds it until the process exits.
+ * workspace (32 MiB).  A device holds it from the first
+ * wf_paged_decode_static_scratch call on that device until the process exits.
  */
 #define WF_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -219,12 +220,19 @@ wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const v
  * WF_STATIC_SCRATCH_BYTES instead, and it allocates nothing (no cudaMalloc,
  * no cudaFree, no allocating library call).
  *
- *   - Returns WF_ERR_WORKSPACE, before launching anything, when the batch needs
- *     more than WF_STATIC_SCRATCH_BYTES (compare
- *     wf_paged_decode_workspace_size(B, num_q_heads, max_seq_len, pool)).
+ *   - Arguments are checked as wf_paged_decode checks them, first: an invalid
+ *     one returns that call's status.  A valid batch that needs more than
+ *     WF_STATIC_SCRATCH_BYTES (compare wf_paged_decode_workspace_size(B,
+ *     num_q_heads, max_seq_len, pool)) returns WF_ERR_WORKSPACE.  Either way
+ *     nothing is launched.
  *   - The first call on a device looks up the array's device address with that
- *     device current (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture.
+ *     device current (cudaGetSymbolAddress) and caches it.  Under CUDA's default
+ *     lazy module loading that lookup is also what maps the array on the device,
+ *     so the device's memory use grows by WF_STATIC_SCRATCH_BYTES at that first
+ *     call and not before.  Make that first call before any stream capture.
+ *   - A device reset (cudaDeviceReset, or the primary context destroyed and
+ *     created again) invalidates the cached address: do not call this entry
+ *     point on a device after resetting it.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls that overlap in
  *     time on the same device, e.g. on two streams, race on it and give wrong
@@ -236,6 +244,21 @@ wf_status wf_paged_decode_static_scratch(void* out, const void* q, const void* k
                                          int32_t B, int32_t max_seq_len, int32_t num_q_heads,
                                          float scale, wf_pool_desc pool, uint32_t* dev_status,
                                          cudaStream_t stream);
+
+/*
+ * Which kernel wf_paged_decode / wf_paged_prefill runs for a pool geometry and
+ * query-head count (host-only, no CUDA call; for tests and tooling).  Returns a
+ * wf_kernel value; WF_KERNEL_NONE when the geometry is invalid or unsupported.
+ */
+typedef enum wf_kernel {
+    WF_KERNEL_NONE = 0,
+    WF_KERNEL_CUDA_CORES = 1,            /* decode: split-K kernel on the CUDA cores          */
+    WF_KERNEL_TENSOR_CORES = 2,          /* decode: split-K tcgen05 kernel (bf16, or fp8 codes);
+                                            prefill: warp-specialised pipelined tcgen05 kernel */
+    WF_KERNEL_TENSOR_CORES_SIMPLE = 3    /* prefill: single-stage tcgen05 kernel (any P)       */
+} wf_kernel;
+int wf_paged_decode_kernel(wf_pool_desc pool, int32_t num_q_heads);
+int wf_paged_prefill_kernel(wf_pool_desc pool, int32_t num_q_heads);
 
 /*
  * Wait for `stream`, copy *dev_status to *host_status and, if clear != 0, reset

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(PKG, "libwf.so")
 WF_OK, WF_ERR_INVALID_ARG, WF_ERR_UNSUPPORTED, WF_ERR_WORKSPACE, WF_ERR_CUDA, WF_ERR_NO_BLOCKS = range(6)
 WF_DTYPE_F32, WF_DTYPE_BF16, WF_DTYPE_FP8_E4M3 = 0, 1, 2
 WF_DEV_BAD_SLOT, WF_DEV_BAD_BLOCK, WF_DEV_BAD_SEQLEN, WF_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+WF_KERNEL_NONE, WF_KERNEL_CUDA_CORES, WF_KERNEL_TENSOR_CORES, WF_KERNEL_TENSOR_CORES_SIMPLE = range(4)
 
 # every entry point include/*.h declares
 EXPORTS = (
@@ -26,6 +27,8 @@ EXPORTS = (
     "wf_paged_decode",
     "wf_paged_prefill",
     "wf_paged_decode_static_scratch",
+    "wf_paged_decode_kernel",
+    "wf_paged_prefill_kernel",
     "wf_device_status_fetch",
     "wf_status_string",
     "wf_abi_version",
@@ -83,6 +86,10 @@ def load(path: str = LIB_PATH):
         lib.wf_paged_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, f32,
                                                        wf_pool_desc, vp, vp]
         lib.wf_paged_decode_static_scratch.restype = ctypes.c_int
+        lib.wf_paged_decode_kernel.argtypes = [wf_pool_desc, i32]
+        lib.wf_paged_decode_kernel.restype = ctypes.c_int
+        lib.wf_paged_prefill_kernel.argtypes = [wf_pool_desc, i32]
+        lib.wf_paged_prefill_kernel.restype = ctypes.c_int
         lib.wf_device_status_fetch.argtypes = [vp, vp, ctypes.c_int, vp]
         lib.wf_device_status_fetch.restype = ctypes.c_int
         lib.wf_status_string.argtypes = [ctypes.c_int]
@@ -252,6 +259,16 @@ def wf_paged_decode_static_scratch(out, q, k_pool, v_pool, block_tables, seq_len
                                             int(H_q), float(scale), pool_desc(k_pool), _ptr(dev_status),
                                             _stream(stream))
     _check("wf_paged_decode_static_scratch", rc)
+
+
+def wf_paged_decode_kernel(desc: wf_pool_desc, num_q_heads: int) -> int:
+    """The WF_KERNEL_* value of the kernel wf_paged_decode runs for this geometry."""
+    return int(load().wf_paged_decode_kernel(desc, int(num_q_heads)))
+
+
+def wf_paged_prefill_kernel(desc: wf_pool_desc, num_q_heads: int) -> int:
+    """The WF_KERNEL_* value of the kernel wf_paged_prefill runs for this geometry."""
+    return int(load().wf_paged_prefill_kernel(desc, int(num_q_heads)))
 
 
 def wf_device_status_fetch(dev_status, clear: bool = True, stream=None) -> int:

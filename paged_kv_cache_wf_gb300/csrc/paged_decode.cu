@@ -736,6 +736,15 @@ bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeomet
     return true;
 }
 
+int decode_kernel_kind(const wf_pool_desc& pool, int32_t num_q_heads) {
+    DecodeGeometry g;
+    if (!decode_geometry(pool, num_q_heads, &g)) return WF_KERNEL_NONE;
+    const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
+    if (decode_tc_supported(pool, num_q_heads) && slots <= INT32_MAX) return WF_KERNEL_TENSOR_CORES;
+    if (pool.dtype == WF_DTYPE_FP8_E4M3 && fp8_on_tensor_cores(pool, num_q_heads)) return WF_KERNEL_TENSOR_CORES;
+    return WF_KERNEL_CUDA_CORES;
+}
+
 size_t decode_workspace_bytes(int32_t B, int32_t num_q_heads, int32_t max_seq_len,
                               const wf_pool_desc& pool) {
     DecodeGeometry g;

@@ -9,11 +9,16 @@
 // cannot provide is the decode workspace.  This file gives them one entry point
 // whose scratch lives in a fixed, file-scope device array instead.
 //
-// The array is WF_STATIC_SCRATCH_BYTES large and exists on every GPU that loads
-// this library, for the life of the process.  Host code cannot use the array's
-// name as a device address (in host code it names a host-side stand-in), so the
-// first call on each device looks up the real address with cudaGetSymbolAddress,
-// with that device current, and caches it per device.
+// The array is WF_STATIC_SCRATCH_BYTES large.  Under CUDA's default lazy module
+// loading it is mapped on a device when this file's module is first loaded
+// there, which the first call on that device does (cudaGetSymbolAddress), and it
+// stays until the process exits or the device's context is destroyed.  Host code
+// cannot use the array's name as a device address (in host code it names a
+// host-side stand-in), so the first call on each device looks up the real
+// address with cudaGetSymbolAddress, with that device current, and caches it per
+// device.  A device reset (cudaDeviceReset, or the primary context destroyed and
+// made again) reloads the module, possibly elsewhere, so the cached address is
+// then stale: callers that reset a device must not use this entry point after.
 #include <mutex>
 
 #include "wf_internal.h"
@@ -52,16 +57,17 @@ extern "C" wf_status wf_paged_decode_static_scratch(
     void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t B, int32_t max_seq_len, int32_t num_q_heads,
     float scale, wf_pool_desc pool, uint32_t* dev_status, cudaStream_t stream) {
-    // Same argument rules as wf_paged_decode; the workspace is the static array.
+    // Same argument rules as wf_paged_decode, checked first: given no workspace it
+    // launches nothing and returns WF_OK (empty batch), an argument error, or
+    // WF_ERR_WORKSPACE for a valid batch.
+    const wf_status pre = wf_paged_decode(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B,
+                                          max_seq_len, num_q_heads, scale, pool, nullptr, 0, dev_status, stream);
+    if (pre != WF_ERR_WORKSPACE) return pre;
+    // a valid batch: it must fit the static array
     const size_t need = wf_paged_decode_workspace_size(B, num_q_heads, max_seq_len, pool);
-    if (B > 0 && need > (size_t)WF_STATIC_SCRATCH_BYTES) return WF_ERR_WORKSPACE;
-    // need == 0 means the arguments are invalid: wf_paged_decode reports which.
+    if (need == 0 || need > (size_t)WF_STATIC_SCRATCH_BYTES) return WF_ERR_WORKSPACE;
     void* scratch = nullptr;
-    if (B > 0 && need > 0) {
-        cudaError_t err = scratch_address(&scratch);
-        if (err != cudaSuccess) return WF_ERR_CUDA;
-    }
+    if (scratch_address(&scratch) != cudaSuccess) return WF_ERR_CUDA;
     return wf_paged_decode(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B, max_seq_len,
-                           num_q_heads, scale, pool, scratch, scratch ? (size_t)WF_STATIC_SCRATCH_BYTES : 0,
-                           dev_status, stream);
+                           num_q_heads, scale, pool, scratch, (size_t)WF_STATIC_SCRATCH_BYTES, dev_status, stream);
 }

@@ -277,6 +277,14 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+int prefill_kernel_kind(const wf_pool_desc& pool, int32_t num_q_heads) {
+    if (pool.dtype != WF_DTYPE_BF16 || (pool.head_dim != 64 && pool.head_dim != 128)) return WF_KERNEL_NONE;
+    if (pool.num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % pool.num_kv_heads != 0) return WF_KERNEL_NONE;
+    if (prefill_tc_supported(pool, num_q_heads) && (int64_t)pool.num_blocks * pool.block_size <= INT32_MAX)
+        return WF_KERNEL_TENSOR_CORES;
+    return WF_KERNEL_TENSOR_CORES_SIMPLE;
+}
+
 cudaError_t launch_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
                                  const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,

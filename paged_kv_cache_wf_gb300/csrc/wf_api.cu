@@ -116,7 +116,7 @@ wf_status from_cuda(cudaError_t e) {
 
 extern "C" {
 
-int wf_abi_version(void) { return 102; }
+int wf_abi_version(void) { return 103; }
 
 const char* wf_status_string(wf_status s) {
     switch (s) {
@@ -215,6 +215,16 @@ wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const v
     return from_cuda(wf::launch_paged_prefill(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
                                               seq_lens, cu_q_lens, B, total_q, max_q_len, max_seq_len,
                                               num_q_heads, scale, pool, dev_status, stream));
+}
+
+int wf_paged_decode_kernel(wf_pool_desc pool, int32_t num_q_heads) {
+    if (check_pool(pool) != WF_OK || num_q_heads < 1) return WF_KERNEL_NONE;
+    return wf::decode_kernel_kind(pool, num_q_heads);
+}
+
+int wf_paged_prefill_kernel(wf_pool_desc pool, int32_t num_q_heads) {
+    if (check_pool(pool) != WF_OK || num_q_heads < 1) return WF_KERNEL_NONE;
+    return wf::prefill_kernel_kind(pool, num_q_heads);
 }
 
 wf_status wf_device_status_fetch(uint32_t* dev_status, uint32_t* host_status, int clear,

@@ -56,6 +56,8 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
                                 const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                                 int32_t num_q_heads, float scale, const wf_pool_desc& pool,
                                 void* workspace, uint32_t* dev_status, cudaStream_t stream);
+// The wf_kernel value of the decode kernel launch_paged_decode picks for this geometry.
+int decode_kernel_kind(const wf_pool_desc& pool, int32_t num_q_heads);
 
 // Tensor-core decode (bf16, D = 128, P % 16 == 0); writes outputs or split
 // partials exactly like the CUDA-core kernel, whose combine kernel finishes it.
@@ -107,6 +109,8 @@ cudaError_t launch_paged_prefill_tc(void* out, const void* q, const void* k_pool
                                     int32_t num_q_heads, float scale, const wf_pool_desc& pool,
                                     uint32_t* dev_status, cudaStream_t stream);
 
+// The wf_kernel value of the prefill kernel launch_paged_prefill picks.
+int prefill_kernel_kind(const wf_pool_desc& pool, int32_t num_q_heads);
 cudaError_t launch_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
                                  const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,

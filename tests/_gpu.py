@@ -14,6 +14,25 @@ TOL = {
 }
 
 
+def geom_desc(geom) -> "wf.wf_pool_desc":
+    """The C pool descriptor of a workload geometry (no device memory needed)."""
+    code = {W.F32: wf.WF_DTYPE_F32, W.BF16: wf.WF_DTYPE_BF16}.get(geom.dtype, wf.WF_DTYPE_FP8_E4M3)
+    return wf.wf_pool_desc(geom.N, geom.P, geom.H_kv, geom.D, code, 1.0, 1.0)
+
+
+def decode_kernel(geom, dtype_code=None) -> int:
+    """WF_KERNEL_* of the kernel wf_paged_decode runs for this geometry."""
+    d = geom_desc(geom)
+    if dtype_code is not None:
+        d.dtype = dtype_code
+    return wf.wf_paged_decode_kernel(d, geom.H_q)
+
+
+def prefill_kernel(geom) -> int:
+    """WF_KERNEL_* of the kernel wf_paged_prefill runs for this geometry."""
+    return wf.wf_paged_prefill_kernel(geom_desc(geom), geom.H_q)
+
+
 def torch_mod():
     import torch
     return torch

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.wf_abi_version() == 102
+    assert lib.wf_abi_version() == 103
     for code in range(6):
         assert wf.status_string(code)
 
@@ -210,3 +210,22 @@ def test_fp8_per_head_scale_checks(lib):
     import torch
     d = wf.pool_desc(torch.empty((2, 16, 8, 128), dtype=torch.uint8), good, 0.25)
     assert d.dtype == wf.WF_DTYPE_FP8_E4M3 and abs(d.k_head_scales[7] - 0.08) < 1e-7 and not d.v_head_scales
+
+
+def test_static_scratch_checks_arguments_before_its_size_limit(lib):
+    """wf_paged_decode_static_scratch applies wf_paged_decode's argument rules
+    first; only a valid batch over WF_STATIC_SCRATCH_BYTES gets WF_ERR_WORKSPACE.
+    None of these calls launches anything."""
+    f = lib.wf_paged_decode_static_scratch
+    d = _desc(N=4000, P=16, H=8, D=128)
+    B, M, msl = 4096, 512, 8192          # far over the 32 MiB array
+    assert wf.wf_paged_decode_workspace_size(B, 32, msl, d) > wf.WF_STATIC_SCRATCH_BYTES
+    args = lambda scale, msl=msl, m=M, ptr=FAKE: (ptr, ptr, ptr, ptr, ptr, m, ptr, B, msl, 32, scale, d, None, None)
+    assert f(*args(0.088)) == wf.WF_ERR_WORKSPACE
+    assert f(*args(float("nan"))) == wf.WF_ERR_INVALID_ARG                 # non-finite scale
+    assert f(*args(0.088, msl=M * 16 + 1)) == wf.WF_ERR_INVALID_ARG        # max_seq_len > M * P
+    assert f(*args(0.088, m=0)) == wf.WF_ERR_INVALID_ARG                   # no table columns
+    assert f(*args(0.088, ptr=FAKE + 4)) == wf.WF_ERR_INVALID_ARG          # misaligned pointers
+    assert f(*args(0.088, ptr=None)) == wf.WF_ERR_INVALID_ARG              # null pointers
+    empty = (None, None, None, None, None, 1, None, 0, 16, 32, 0.088, d, None, None)
+    assert f(*empty) == wf.WF_OK                                            # empty batch: no-op

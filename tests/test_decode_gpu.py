@@ -46,6 +46,14 @@ CASES = {
     "gqa4_D128_items256": lambda: W.custom_layout(32, 8, 128, 16, W.BF16,
                                                   [255, 256, 257, 511, 512, 513, 768, 769], seed=16),
     "mha12_items64": lambda: W.custom_layout(12, 12, 64, 16, W.BF16, [63, 64, 65, 128, 129, 193], seed=17),
+    # tensor-core decode, group of 2 at D = 128 (H_q = 16, H_kv = 8)
+    "gqa2_D128_ragged": lambda: W.custom_layout(16, 8, 128, 16, W.BF16,
+                                                [1, 15, 16, 17, 255, 256, 257, 1000, 3001], seed=18),
+    # tensor-core decode at D = 128 with blocks of 32 and 64 positions (a 16-position
+    # tile is a sub-range of one block)
+    "gqa4_D128_P32": lambda: W.custom_layout(32, 8, 128, 32, W.BF16, [1, 31, 32, 33, 300, 2049], seed=19),
+    "gqa4_D128_P64": lambda: W.custom_layout(32, 8, 128, 64, W.BF16, [1, 63, 64, 65, 700, 1500], seed=20),
+    "gqa2_D128_P64": lambda: W.custom_layout(16, 8, 128, 64, W.BF16, [2, 64, 129, 513, 1200], seed=21),
 }
 
 
@@ -69,25 +77,32 @@ def test_decode_matches_oracle(name):
 
 
 def test_decode_block_size_invariance():
-    """Same values by position, paged with P in {1,2,3,7,16,32,64}.
+    """The same values by position, paged with P in {1, 2, 3, 7, 16, 32, 64}.
 
-    Block sizes that are multiples of 16 take the tensor-core kernel (bf16, D=128),
-    the others the CUDA-core kernel; within each kernel the bytes out are identical
-    for every P, and the two kernels agree within the bf16 tolerance."""
-    sl = [1, 17, 130, 300]
+    Llama-3-8B heads (H_q 32, H_kv 8, D 128, bf16): block sizes that are multiples of
+    16 run the tensor-core kernel, the others the CUDA-core kernel.  Every P is
+    compared with the oracle, and within each kernel the output bytes are identical
+    for every P: the tile order depends only on the logical position."""
+    sl = [1, 17, 130, 300, 1025]
     outs = {}
     base = None
+    ref = None
     for P in (1, 2, 3, 7, 16, 32, 64):
-        lay = W.custom_layout(8, 2, 128, P, W.BF16, sl, seed=P)
+        lay = W.custom_layout(32, 8, 128, P, W.BF16, sl, seed=P)
+        want = wf.WF_KERNEL_TENSOR_CORES if P % 16 == 0 else wf.WF_KERNEL_CUDA_CORES
+        assert G.decode_kernel(lay.geom) == want, P
         if base is None:
             base = W.draw_layer_values(lay, np.random.default_rng(8))
-        pools = G.build_dev_pools(lay, base)
-        outs[P] = G.run_decode(lay, base, pools, 0.088)
+            ref = _oracle_decode(lay, base, 0.088)
+        st = G.dev_status()
+        pools = G.build_dev_pools(lay, base, st)
+        outs[P] = G.run_decode(lay, base, pools, 0.088, st)
+        assert wf.wf_device_status_fetch(st) == 0
+        G.assert_close(G.from_dev(outs[P], W.BF16), ref, W.BF16, f"P={P}")
     for fam in ((1, 2, 3, 7), (16, 32, 64)):
-        ref = G.storage_bytes(outs[fam[0]])
+        first = G.storage_bytes(outs[fam[0]])
         for P in fam[1:]:
-            assert np.array_equal(G.storage_bytes(outs[P]), ref), P
-    G.assert_close(G.from_dev(outs[16], W.BF16), G.from_dev(outs[1], W.BF16), W.BF16, "tensor vs CUDA cores")
+            assert np.array_equal(G.storage_bytes(outs[P]), first), P
 
 
 def test_decode_batch_invariance_bit_identical():

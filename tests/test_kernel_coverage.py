@@ -1,0 +1,72 @@
+"""Every instance of the tensor-core kernels meets the oracle in some GPU case.
+
+Host-only: asks libwf which kernel each GPU parity case reaches
+(wf_paged_decode_kernel / wf_paged_prefill_kernel, no CUDA call) and checks that
+the cases name every (group size G, head dim D) instance of the tensor-core
+decode and prefill kernels, and the block sizes that change how a tile maps onto
+a block (P = 16, 32 and 64 at D = 128).
+"""
+import pytest
+
+from paged_kv_cache_wf_gb300 import binding as wf
+from tests import _gpu as G
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return wf.load()
+
+
+def _decode_cases():
+    from tests import test_decode_gpu, test_fp8_gpu
+    bf = {n: f().geom for n, f in test_decode_gpu.CASES.items()}
+    f8 = {n: f().geom for n, f in test_fp8_gpu.CASES.items()}
+    return bf, f8
+
+
+def test_bf16_decode_cases_reach_every_tensor_core_instance(lib):
+    bf, _ = _decode_cases()
+    reached = set()
+    for name, g in bf.items():
+        if G.decode_kernel(g) == wf.WF_KERNEL_TENSOR_CORES:
+            reached.add((g.H_q // g.H_kv, g.D))
+    assert {(2, 64), (4, 64), (2, 128), (4, 128)} <= reached, reached
+    p128 = {g.P for g in bf.values() if G.decode_kernel(g) == wf.WF_KERNEL_TENSOR_CORES and g.D == 128}
+    assert {16, 32, 64} <= p128, p128
+
+
+def test_fp8_decode_cases_reach_every_tensor_core_instance(lib):
+    _, f8 = _decode_cases()
+    reached = set()
+    for g in f8.values():
+        if G.decode_kernel(g, wf.WF_DTYPE_FP8_E4M3) == wf.WF_KERNEL_TENSOR_CORES:
+            reached.add((g.H_q // g.H_kv, g.D))
+    assert {(2, 128), (4, 128)} <= reached, reached
+    assert any(G.decode_kernel(g, wf.WF_DTYPE_FP8_E4M3) == wf.WF_KERNEL_CUDA_CORES for g in f8.values())
+
+
+def test_prefill_cases_reach_every_tensor_core_instance(lib):
+    from paged_kv_cache_wf_gb300 import workloads as W
+    from tests import test_prefill_gpu
+    reached, simple = set(), 0
+    for name, (H_q, H_kv, D, P, sl, ql) in test_prefill_gpu.CASES.items():
+        g = W.custom_layout(H_q, H_kv, D, P, W.BF16, sl, ql, seed=len(name)).geom
+        k = G.prefill_kernel(g)
+        if k == wf.WF_KERNEL_TENSOR_CORES:
+            reached.add((H_q // H_kv, D))
+        elif k == wf.WF_KERNEL_TENSOR_CORES_SIMPLE:
+            simple += 1
+    want = {(gs, d) for gs in (1, 2, 4, 8) for d in (64, 128)}
+    assert want <= reached, want - reached
+    assert simple >= 2
+
+
+def test_kernel_query_rejects_invalid_geometry(lib):
+    d = wf.wf_pool_desc(16, 16, 8, 96, wf.WF_DTYPE_BF16, 1.0, 1.0)
+    assert wf.wf_paged_decode_kernel(d, 32) == wf.WF_KERNEL_NONE
+    d = wf.wf_pool_desc(16, 16, 8, 128, wf.WF_DTYPE_BF16, 1.0, 1.0)
+    assert wf.wf_paged_decode_kernel(d, 12) == wf.WF_KERNEL_NONE   # 12 % 8 != 0
+    assert wf.wf_paged_decode_kernel(d, 32) == wf.WF_KERNEL_TENSOR_CORES
+    d.dtype = wf.WF_DTYPE_F32
+    assert wf.wf_paged_decode_kernel(d, 32) == wf.WF_KERNEL_CUDA_CORES
+    assert wf.wf_paged_prefill_kernel(d, 32) == wf.WF_KERNEL_NONE   # prefill is bf16 only

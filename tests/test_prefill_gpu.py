@@ -33,6 +33,10 @@ CASES = {
     "P1_P3_odd": (6, 3, 128, 3, [129, 257], [129, 2]),
     "gqa8": (16, 2, 128, 64, [333, 64], [200, 64]),
     "empty_request_in_batch": (4, 2, 128, 16, [50, 60, 70], [10, 0, 70]),
+    # D = 64 instances of the pipelined tensor-core kernel at every group size
+    "D64_mha_gpt2": (12, 12, 64, 16, [300, 129, 40], [300, 64, 40]),
+    "D64_gqa2": (16, 8, 64, 16, [520, 77], [260, 77]),
+    "D64_gqa8": (16, 2, 64, 32, [333, 64, 1], [200, 64, 1]),
 }
 
 
