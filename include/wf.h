@@ -69,7 +69,9 @@ typedef enum wf_dtype {
 #define WF_DEV_BAD_BLOCK   0x2u  /* block id outside [0, N): that block's rows were skipped  */
 #define WF_DEV_BAD_SEQLEN  0x4u  /* seq_lens[b] < 1, > max_seq_len, > M*P, or < q_len:
                                     sequence b was skipped and its output left unwritten    */
-#define WF_DEV_TIMEOUT     0x8u  /* an internal pipeline wait gave up (should never happen) */
+#define WF_DEV_TIMEOUT     0x8u  /* a wait gave up: an internal pipeline wait (should never
+                                    happen), or a decode worker idle past its limit          */
+#define WF_DEV_BAD_TASK    0x10u /* decode worker: a task record out of range (skipped)     */
 
 /* One layer's pool geometry.  k_pool and v_pool are each [N, P, H_kv, D]. */
 typedef struct wf_pool_desc {
@@ -244,6 +246,67 @@ wf_status wf_paged_decode_static_scratch(void* out, const void* q, const void* k
                                          int32_t B, int32_t max_seq_len, int32_t num_q_heads,
                                          float scale, wf_pool_desc pool, uint32_t* dev_status,
                                          cudaStream_t stream);
+
+/*
+ * wf_decode_worker -- a persistent decode worker that takes tasks while it runs.
+ * (Awesome System Papers wiki, WEAVER summary, "核心方法": a receiver kernel spins
+ *  on a task counter, runs the attention it finds and bumps a completion counter,
+ *  so no host launch sits between a request and its attention.)
+ *
+ * The worker grid (num_workers CTAs of 256 threads) is launched once on `stream`.
+ * A feeder outside it -- typically a host thread issuing cudaMemcpyAsync on
+ * another non-blocking stream, so the copy engine writes while the worker runs --
+ * appends task records to `tasks` and then raises mailbox->posted.  Each CTA
+ * claims the next task index (one atomic increment of mailbox->claimed), waits
+ * until that task is posted, decodes it and, once its output is written,
+ * increments mailbox->done.
+ *
+ *   tasks      device array of task_capacity records; task t lives in tasks[t].
+ *              Write a record before raising `posted` past it (e.g. its copy
+ *              earlier on the same stream as the copy of `posted`).
+ *   mailbox    device memory (16-byte aligned):
+ *                posted   feeder: tasks 0 .. posted-1 are readable (<= task_capacity)
+ *                stop     feeder: nonzero = leave once every posted task is claimed;
+ *                         write it after the last `posted`
+ *                claimed  worker: next task to claim
+ *                done     worker: tasks whose outputs are written
+ *              The call zeroes `claimed` and `done` on `stream` before the worker
+ *              starts; `posted` and `stop` are the feeder's (zero them before).
+ *   task       {seq_len, table_row, q_row, out_row}: out[out_row] = decode of
+ *              q[q_row] over positions 0 .. seq_len-1 mapped by
+ *              block_tables[table_row] (the computation of wf_paged_decode for
+ *              one sequence).  Records with an index out of range are skipped
+ *              and flagged WF_DEV_BAD_TASK (they still count as done).
+ *   out, q     [num_rows, H_q, D] of the pool dtype (float32 or bfloat16 pools)
+ *   block_tables [num_table_rows, max_blocks_per_seq] int32
+ *   idle_timeout_ns  longest time a CTA waits for its claimed task; past it the
+ *              CTA sets WF_DEV_TIMEOUT in *dev_status and returns, leaving its
+ *              task unrun.  While a CTA waits it has no copy or tensor-core
+ *              operation in flight.
+ * The worker holds num_workers CTAs until it stops or times out: anything that
+ * waits for the whole device (cudaDeviceSynchronize, cudaMalloc/cudaFree in many
+ * allocators) blocks until then, so a feeder must not call such things.
+ * fp8 pools: WF_ERR_UNSUPPORTED.
+ */
+typedef struct wf_worker_mailbox {
+    uint32_t posted;
+    uint32_t stop;
+    uint32_t claimed;
+    uint32_t done;
+} wf_worker_mailbox;
+
+typedef struct wf_decode_task {
+    int32_t seq_len;
+    int32_t table_row;
+    int32_t q_row;
+    int32_t out_row;
+} wf_decode_task;
+
+wf_status wf_decode_worker(void* out, const void* q, int32_t num_rows, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, int32_t num_table_rows, int32_t max_blocks_per_seq,
+                           int32_t num_q_heads, float scale, wf_pool_desc pool, const wf_decode_task* tasks,
+                           int32_t task_capacity, wf_worker_mailbox* mailbox, int32_t num_workers,
+                           uint64_t idle_timeout_ns, uint32_t* dev_status, cudaStream_t stream);
 
 /*
  * Which kernel wf_paged_decode / wf_paged_prefill runs for a pool geometry and

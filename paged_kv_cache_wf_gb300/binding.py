@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(PKG, "libwf.so")
 
 WF_OK, WF_ERR_INVALID_ARG, WF_ERR_UNSUPPORTED, WF_ERR_WORKSPACE, WF_ERR_CUDA, WF_ERR_NO_BLOCKS = range(6)
 WF_DTYPE_F32, WF_DTYPE_BF16, WF_DTYPE_FP8_E4M3 = 0, 1, 2
-WF_DEV_BAD_SLOT, WF_DEV_BAD_BLOCK, WF_DEV_BAD_SEQLEN, WF_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+WF_DEV_BAD_SLOT, WF_DEV_BAD_BLOCK, WF_DEV_BAD_SEQLEN, WF_DEV_TIMEOUT, WF_DEV_BAD_TASK = 0x1, 0x2, 0x4, 0x8, 0x10
 WF_KERNEL_NONE, WF_KERNEL_CUDA_CORES, WF_KERNEL_TENSOR_CORES, WF_KERNEL_TENSOR_CORES_SIMPLE = range(4)
 
 # every entry point include/*.h declares
@@ -27,6 +27,7 @@ EXPORTS = (
     "wf_paged_decode",
     "wf_paged_prefill",
     "wf_paged_decode_static_scratch",
+    "wf_decode_worker",
     "wf_paged_decode_kernel",
     "wf_paged_prefill_kernel",
     "wf_device_status_fetch",
@@ -86,6 +87,9 @@ def load(path: str = LIB_PATH):
         lib.wf_paged_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, f32,
                                                        wf_pool_desc, vp, vp]
         lib.wf_paged_decode_static_scratch.restype = ctypes.c_int
+        lib.wf_decode_worker.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, wf_pool_desc, vp, i32, vp,
+                                         i32, ctypes.c_uint64, vp, vp]
+        lib.wf_decode_worker.restype = ctypes.c_int
         lib.wf_paged_decode_kernel.argtypes = [wf_pool_desc, i32]
         lib.wf_paged_decode_kernel.restype = ctypes.c_int
         lib.wf_paged_prefill_kernel.argtypes = [wf_pool_desc, i32]
@@ -259,6 +263,25 @@ def wf_paged_decode_static_scratch(out, q, k_pool, v_pool, block_tables, seq_len
                                             int(H_q), float(scale), pool_desc(k_pool), _ptr(dev_status),
                                             _stream(stream))
     _check("wf_paged_decode_static_scratch", rc)
+
+
+def wf_decode_worker(out, q, k_pool, v_pool, block_tables, tasks, mailbox, scale: float, num_workers: int,
+                     idle_timeout_ns: int, dev_status=None, stream=None):
+    """Launch the persistent decode worker (returns at once; the grid runs until the
+    feeder sets stop or a CTA idles past idle_timeout_ns).  out, q [rows, H_q, D];
+    block_tables [table_rows, M] int32; tasks [capacity, 4] int32 records
+    (seq_len, table_row, q_row, out_row); mailbox [4] 32-bit words (posted, stop,
+    claimed, done), all on the device."""
+    _contig(out, q, k_pool, v_pool, block_tables, tasks, mailbox)
+    if tasks.dim() != 2 or tasks.shape[1] != 4 or mailbox.numel() != 4:
+        raise ValueError("tasks must be [capacity, 4] int32 and mailbox 4 words")
+    lib = load()
+    rows, H_q, _ = q.shape
+    rc = lib.wf_decode_worker(_ptr(out), _ptr(q), int(rows), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                              int(block_tables.shape[0]), int(block_tables.shape[1]), int(H_q), float(scale),
+                              pool_desc(k_pool), _ptr(tasks), int(tasks.shape[0]), _ptr(mailbox), int(num_workers),
+                              int(idle_timeout_ns), _ptr(dev_status), _stream(stream))
+    _check("wf_decode_worker", rc)
 
 
 def wf_paged_decode_kernel(desc: wf_pool_desc, num_q_heads: int) -> int:

@@ -217,6 +217,31 @@ wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const v
                                               num_q_heads, scale, pool, dev_status, stream));
 }
 
+wf_status wf_decode_worker(void* out, const void* q, int32_t num_rows, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, int32_t num_table_rows, int32_t max_blocks_per_seq,
+                           int32_t num_q_heads, float scale, wf_pool_desc pool, const wf_decode_task* tasks,
+                           int32_t task_capacity, wf_worker_mailbox* mailbox, int32_t num_workers,
+                           uint64_t idle_timeout_ns, uint32_t* dev_status, cudaStream_t stream) {
+    wf_status s = check_pool(pool);
+    if (s != WF_OK) return s;
+    if (pool.dtype == WF_DTYPE_FP8_E4M3) return WF_ERR_UNSUPPORTED;
+    if (num_rows < 0 || num_table_rows < 0 || max_blocks_per_seq < 1 || num_q_heads < 1 || task_capacity < 0)
+        return WF_ERR_INVALID_ARG;
+    if (num_q_heads % pool.num_kv_heads != 0) return WF_ERR_INVALID_ARG;
+    if (num_q_heads / pool.num_kv_heads > 8) return WF_ERR_UNSUPPORTED;
+    if (num_workers < 1 || num_workers > 4096 || idle_timeout_ns == 0) return WF_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return WF_ERR_INVALID_ARG;
+    if (!mailbox || (reinterpret_cast<uintptr_t>(mailbox) & 15u)) return WF_ERR_INVALID_ARG;
+    if (task_capacity > 0 && (!tasks || (reinterpret_cast<uintptr_t>(tasks) & 15u))) return WF_ERR_INVALID_ARG;
+    if (num_rows > 0 && (!out || !q || !aligned16(out) || !aligned16(q))) return WF_ERR_INVALID_ARG;
+    if (!k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool)) return WF_ERR_INVALID_ARG;
+    if (num_table_rows > 0 && (!block_tables || (reinterpret_cast<uintptr_t>(block_tables) & 3u)))
+        return WF_ERR_INVALID_ARG;
+    return from_cuda(wf::launch_decode_worker(out, q, num_rows, k_pool, v_pool, block_tables, num_table_rows,
+                                              max_blocks_per_seq, num_q_heads, scale, pool, tasks, task_capacity,
+                                              mailbox, num_workers, idle_timeout_ns, dev_status, stream));
+}
+
 int wf_paged_decode_kernel(wf_pool_desc pool, int32_t num_q_heads) {
     if (check_pool(pool) != WF_OK || num_q_heads < 1) return WF_KERNEL_NONE;
     return wf::decode_kernel_kind(pool, num_q_heads);

@@ -99,6 +99,14 @@ inline HeadScales head_scales(const wf_pool_desc& pool) {
 // Workspace the fp8 decode needs beyond the partials: the prepared q parts and scales.
 size_t decode_fp8_prep_bytes(int32_t B, int32_t num_q_heads);
 
+// Persistent decode worker fed while it runs (decode_worker.cu).
+cudaError_t launch_decode_worker(void* out, const void* q, int32_t num_rows, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_tables, int32_t num_table_rows, int32_t max_blocks_per_seq,
+                                 int32_t num_q_heads, float scale, const wf_pool_desc& pool,
+                                 const wf_decode_task* tasks, int32_t task_capacity, wf_worker_mailbox* mailbox,
+                                 int32_t num_workers, uint64_t idle_timeout_ns, uint32_t* dev_status,
+                                 cudaStream_t stream);
+
 // ---- prefill ------------------------------------------------------------------
 // Pipelined tcgen05 prefill (bf16, P % 16 == 0, G in {1, 2, 4, 8}, D in {64, 128}).
 bool prefill_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads);

@@ -229,3 +229,21 @@ def test_static_scratch_checks_arguments_before_its_size_limit(lib):
     assert f(*args(0.088, ptr=None)) == wf.WF_ERR_INVALID_ARG              # null pointers
     empty = (None, None, None, None, None, 1, None, 0, 16, 32, 0.088, d, None, None)
     assert f(*empty) == wf.WF_OK                                            # empty batch: no-op
+
+
+def test_decode_worker_argument_checks(lib):
+    f = lib.wf_decode_worker
+    d = _desc(N=10, P=16, H=2, D=64)
+    ok = lambda **kw: dict(dict(out=FAKE, q=FAKE, rows=4, kp=FAKE, vp=FAKE, bt=FAKE, trows=4, M=2, hq=4, scale=0.1,
+                                pool=d, tasks=FAKE, cap=8, mb=FAKE, workers=2, timeout=10**6), **kw)
+    call = lambda a: f(a["out"], a["q"], a["rows"], a["kp"], a["vp"], a["bt"], a["trows"], a["M"], a["hq"],
+                       a["scale"], a["pool"], a["tasks"], a["cap"], a["mb"], a["workers"], a["timeout"], None, None)
+    assert call(ok(mb=None)) == wf.WF_ERR_INVALID_ARG
+    assert call(ok(mb=FAKE + 4)) == wf.WF_ERR_INVALID_ARG            # mailbox not 16-byte aligned
+    assert call(ok(workers=0)) == wf.WF_ERR_INVALID_ARG
+    assert call(ok(timeout=0)) == wf.WF_ERR_INVALID_ARG
+    assert call(ok(hq=3)) == wf.WF_ERR_INVALID_ARG                   # 3 % 2 != 0
+    assert call(ok(hq=18)) == wf.WF_ERR_UNSUPPORTED                  # group of 9
+    assert call(ok(scale=float("inf"))) == wf.WF_ERR_INVALID_ARG
+    assert call(ok(pool=_fp8(N=10, P=16, H=2, D=64))) == wf.WF_ERR_UNSUPPORTED
+    assert call(ok(tasks=None)) == wf.WF_ERR_INVALID_ARG
