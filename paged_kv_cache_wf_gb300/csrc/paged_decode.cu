@@ -725,7 +725,7 @@ bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeomet
     // the tensor-core kernels (bf16, and every fp8 pool) have their own item spans
     g->split_span = pool.dtype == WF_DTYPE_FP8_E4M3
                         ? (fp8_on_tensor_cores(pool, num_q_heads) ? decode_tc_fp8_span() : kSpan)
-                    : decode_tc_supported(pool, num_q_heads) ? decode_tc_span(pool.head_dim)
+                    : decode_tc_supported(pool, num_q_heads) ? decode_tc_span(pool)
                                                              : kSpan;
     g->tile = G > 4 ? 8 : 16;
     g->stages = 0;  // chosen per kernel instance at launch

@@ -120,13 +120,15 @@ struct ItemWalk {
     int total = 0;      // items in the window
 };
 
+// `per` work items share each split (e.g. one per group of KV heads): a sequence
+// of len positions has ceil(len / span) * per items, numbered split-major.
 __device__ __forceinline__ void item_walk_load(ItemWalk& w, const int32_t* seq_lens, int B, int span, int64_t cap,
-                                               uint32_t* status, int lane) {
+                                               uint32_t* status, int lane, int per = 1) {
     const int bb = w.base + lane;
     int n = 0, len = 0;
     if (bb < B) {
         len = __ldg(seq_lens + bb);
-        if (len >= 1 && (int64_t)len <= cap) n = (len + span - 1) / span;
+        if (len >= 1 && (int64_t)len <= cap) n = (len + span - 1) / span * per;
         else report(status, WF_DEV_BAD_SEQLEN);
     }
     w.len = len;
@@ -142,11 +144,11 @@ __device__ __forceinline__ void item_walk_load(ItemWalk& w, const int32_t* seq_l
 }
 
 // Finds item `item` (uniform across the warp): false when it lies past the last
-// sequence, else its sequence b, that sequence's length and split count, and the
-// number of items before the sequence.
+// sequence, else its sequence b, that sequence's length and item count (its split
+// count times `per`), and the number of items before the sequence.
 __device__ __forceinline__ bool item_walk_find(ItemWalk& w, int64_t item, const int32_t* seq_lens, int B, int span,
                                                int64_t cap, uint32_t* status, int lane, int& b, int& len, int& nsp,
-                                               int64_t& cum) {
+                                               int64_t& cum, int per = 1) {
     for (;;) {
         if (w.base >= B) return false;
         if (item < w.cum + w.total) {
@@ -160,7 +162,7 @@ __device__ __forceinline__ bool item_walk_find(ItemWalk& w, int64_t item, const 
         }
         w.cum += w.total;
         w.base += 32;
-        if (w.base < B) item_walk_load(w, seq_lens, B, span, cap, status, lane);
+        if (w.base < B) item_walk_load(w, seq_lens, B, span, cap, status, lane, per);
     }
 }
 
@@ -556,6 +558,19 @@ __device__ __forceinline__ void ld_8cols(uint32_t taddr, float (&v)[8]) {
                  : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void ld_1col(uint32_t taddr, float (&v)[1]) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    v[0] = __uint_as_float(r);
+}
+
+__device__ __forceinline__ void ld_2cols(uint32_t taddr, float (&v)[2]) {
+    uint32_t r[2];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+    v[0] = __uint_as_float(r[0]);
+    v[1] = __uint_as_float(r[1]);
 }
 
 __device__ __forceinline__ void ld_4cols(uint32_t taddr, float (&v)[4]) {

@@ -62,7 +62,7 @@ int decode_kernel_kind(const wf_pool_desc& pool, int32_t num_q_heads);
 // Tensor-core decode (bf16, D = 128, P % 16 == 0); writes outputs or split
 // partials exactly like the CUDA-core kernel, whose combine kernel finishes it.
 bool decode_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads);
-int decode_tc_span(int head_dim);
+int decode_tc_span(const wf_pool_desc& pool);   // positions per split
 cudaError_t launch_paged_decode_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
                                    const int32_t* seq_lens, int32_t B, int32_t max_seq_len,

@@ -54,6 +54,19 @@ CASES = {
     "gqa4_D128_P32": lambda: W.custom_layout(32, 8, 128, 32, W.BF16, [1, 31, 32, 33, 300, 2049], seed=19),
     "gqa4_D128_P64": lambda: W.custom_layout(32, 8, 128, 64, W.BF16, [1, 63, 64, 65, 700, 1500], seed=20),
     "gqa2_D128_P64": lambda: W.custom_layout(16, 8, 128, 64, W.BF16, [2, 64, 129, 513, 1200], seed=21),
+    # tensor-core decode for other KV-head counts: a tile holds 8 / HT boxes of 16
+    # positions of HT heads (HT = the largest power of two <= 8 dividing H_kv)
+    "mha8_D128": lambda: W.custom_layout(8, 8, 128, 16, W.BF16, [1, 17, 255, 256, 257, 900], seed=22),
+    "mha16_D64_two_groups": lambda: W.custom_layout(16, 16, 64, 16, W.BF16, [5, 128, 129, 1000], seed=23),
+    "gqa2_kv16_D128": lambda: W.custom_layout(32, 16, 128, 32, W.BF16, [3, 300, 1100], seed=24),
+    "gqa4_kv2_D128": lambda: W.custom_layout(8, 2, 128, 16, W.BF16, [1, 16, 17, 63, 64, 65, 700, 2000], seed=25),
+    "gqa2_kv6_D64_P32": lambda: W.custom_layout(12, 6, 64, 32, W.BF16, [1, 31, 33, 128, 129, 640], seed=26),
+    "mqa_gqa4_kv1_D128": lambda: W.custom_layout(4, 1, 128, 16, W.BF16, [1, 15, 16, 17, 127, 128, 129, 1500], seed=27),
+    "mqa_kv1_D64": lambda: W.custom_layout(1, 1, 64, 16, W.BF16, [2, 100, 129, 700], seed=28),
+    "gqa2_kv3_D64": lambda: W.custom_layout(6, 3, 64, 16, W.BF16, [1, 44, 128, 300, 1024], seed=29),
+    "gqa4_kv4_D64_P64": lambda: W.custom_layout(16, 4, 64, 64, W.BF16, [64, 65, 128, 129, 1000], seed=30),
+    # a group of 8 stays on the CUDA cores
+    "gqa8_bf16_cuda_cores": lambda: W.custom_layout(16, 2, 128, 16, W.BF16, [1, 300, 1029], seed=31),
 }
 
 

@@ -26,13 +26,24 @@ def _decode_cases():
 
 def test_bf16_decode_cases_reach_every_tensor_core_instance(lib):
     bf, _ = _decode_cases()
-    reached = set()
+    reached, heads_per_box = set(), set()
     for name, g in bf.items():
         if G.decode_kernel(g) == wf.WF_KERNEL_TENSOR_CORES:
             reached.add((g.H_q // g.H_kv, g.D))
-    assert {(2, 64), (4, 64), (2, 128), (4, 128)} <= reached, reached
+            ht = 8
+            while g.H_kv % ht:
+                ht //= 2
+            heads_per_box.add((ht, g.H_kv // ht > 1))
+    assert {(gs, d) for gs in (1, 2, 4) for d in (64, 128)} <= reached, reached
+    # every box shape (HT heads x 16 positions, 8 / HT boxes a tile), with one and
+    # with several head groups per split
+    assert {1, 2, 4, 8} <= {ht for ht, _ in heads_per_box}, heads_per_box
+    assert {True, False} <= {many for _, many in heads_per_box}, heads_per_box
     p128 = {g.P for g in bf.values() if G.decode_kernel(g) == wf.WF_KERNEL_TENSOR_CORES and g.D == 128}
     assert {16, 32, 64} <= p128, p128
+    # groups of 8 and fp32 pools run on the CUDA cores
+    assert any(G.decode_kernel(g) == wf.WF_KERNEL_CUDA_CORES and g.H_q // g.H_kv == 8 and g.dtype == "bf16"
+               for g in bf.values())
 
 
 def test_fp8_decode_cases_reach_every_tensor_core_instance(lib):
