@@ -66,6 +66,7 @@ struct DecodeParams {
     int32_t HG;          // head groups: H_kv / HC
     int32_t split_span;  // positions per split
     int32_t max_splits;
+    int32_t ps_h, ps_s;  // partial-row strides of a query head and a split (partial_row)
     int32_t stages;
     float scale_log2;    // scale * log2(e)
     // fp8 e4m3 pools: the scale of each KV head's K and V codes (a code c of head h
@@ -554,16 +555,16 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kern
                     }
                 }
             } else {
-                const int64_t base = ((int64_t)mt.b * p.max_splits + mt.split) * p.H_q + hq0;
 #pragma unroll
                 for (int g = 0; g < GMAX; ++g) {
                     if (g < G) {
-                        float* dst = p.ws_o + (base + g) * D + dcol;
+                        const int64_t row = partial_row(mt.b, hq0 + g, mt.split, p.H_q, p.max_splits, p.ps_h, p.ps_s);
+                        float* dst = p.ws_o + row * D + dcol;
                         float vsc = 1.f;
                         if constexpr (kCodes) vsc = p.v_head[mt.hg * p.HC + pair];   // partials carry the V scale
 #pragma unroll
                         for (int vv = 0; vv < S::VPL; ++vv) dst[vv] = (acc[g][vv].x + acc[g][vv].y) * vsc;
-                        if (half == 0 && lane == 0) p.ws_ml[base + g] = make_float2(Mh[g], Lh[g]);
+                        if (half == 0 && lane == 0) p.ws_ml[row] = make_float2(Mh[g], Lh[g]);
                     }
                 }
             }
@@ -574,14 +575,16 @@ __global__ void __launch_bounds__((2 * kMaxHC + 1) * 32, MINB) paged_decode_kern
 // Merge the splits of every (sequence, query head) with more than one split:
 //   out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j.
 // One warp per (b, query head); lanes own D/32 output dims.  The merge is bound by
-// the latency of reading the partials, so each lane issues the loads of kBatch
-// splits back to back before using any of them.  Launched as a programmatic
-// dependent of the split kernel: the grid may start while the split kernel drains,
-// and waits for it (griddepcontrol.wait) before reading the workspace.
+// the latency of reading the partials: each round of up to kChunk splits issues
+// its (m, l) loads and every o row load at once, before using any of them, and
+// folds the round in with an online rescale, so a merge of up to kChunk splits is
+// one round trip.  Launched as a programmatic dependent of the split kernel: the
+// grid may start while the split kernel drains, and waits for it
+// (griddepcontrol.wait) before reading the workspace.
 template <typename E, int D>
-__global__ void __launch_bounds__(128, 8) paged_decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128, 4) paged_decode_combine_kernel(const DecodeParams p) {
     constexpr int VPL = D / 32;
-    constexpr int kBatch = 8;
+    constexpr int kChunk = D == 128 ? 24 : 32;       // o rows in flight per lane (<= 96 registers)
     using Vec = typename std::conditional<VPL == 4, float4, float2>::type;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq = blockIdx.x * 4 + warp;
@@ -592,42 +595,42 @@ __global__ void __launch_bounds__(128, 8) paged_decode_combine_kernel(const Deco
     if (!len_ok(len, p)) return;
     const int n = (len + p.split_span - 1) / p.split_span;
     if (n <= 1) return;
-    const int64_t base = (int64_t)b * p.max_splits * p.H_q + hq;  // + j * H_q
-    float mx = -INFINITY;
-    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, p.ws_ml[base + (int64_t)j * p.H_q].x);
-#pragma unroll
-    for (int mask = 16; mask >= 1; mask >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
-    float den = 0.f;
+    const int64_t row0 = partial_row(b, hq, 0, p.H_q, p.max_splits, p.ps_h, p.ps_s);
+    const Vec* orow = reinterpret_cast<const Vec*>(p.ws_o + row0 * D) + lane;   // + j * ps_s * (D / VPL)
+    const float2* mrow = p.ws_ml + row0;                                        // + j * ps_s
+    float M = -INFINITY, den = 0.f;
     float o[VPL];
 #pragma unroll
     for (int k = 0; k < VPL; ++k) o[k] = 0.f;
-    for (int j0 = 0; j0 < n; j0 += 32) {
-        float wl = 0.f;
-        if (j0 + lane < n) {
-            const float2 ml = p.ws_ml[base + (int64_t)(j0 + lane) * p.H_q];
-            wl = exp2f(ml.x - mx);
-            den += wl * ml.y;
-        }
-        const int cnt = min(32, n - j0);
-        for (int jj = 0; jj < cnt; jj += kBatch) {
-            Vec x[kBatch];
+    for (int j0 = 0; j0 < n; j0 += kChunk) {
+        const int cnt = min(kChunk, n - j0);
+        Vec x[kChunk];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (jj + u < cnt)
-                    x[u] = __ldcg(reinterpret_cast<const Vec*>(p.ws_o + (base + (int64_t)(j0 + jj + u) * p.H_q) * D +
-                                                               lane * VPL));
+        for (int u = 0; u < kChunk; ++u)
+            if (u < cnt) x[u] = __ldcg(orow + (int64_t)(j0 + u) * p.ps_s * (D / VPL));
+        const float2 ml = lane < cnt ? __ldcg(mrow + (int64_t)(j0 + lane) * p.ps_s) : make_float2(-INFINITY, 0.f);
+        float cm = ml.x;
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const float w = __shfl_sync(0xffffffffu, wl, (jj + u) & 31);
-                if (jj + u < cnt) {
-                    if constexpr (VPL == 4) {
-                        o[0] += w * x[u].x; o[1] += w * x[u].y; o[2] += w * x[u].z; o[3] += w * x[u].w;
-                    } else {
-                        o[0] += w * x[u].x; o[1] += w * x[u].y;
-                    }
+        for (int mask = 16; mask >= 1; mask >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, mask));
+        const float Mn = fmaxf(M, cm);                     // finite: every split has a live position
+        const float a = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        den *= a;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) o[k] *= a;
+        const float wl = lane < cnt ? exp2f(ml.x - Mn) : 0.f;
+        den += wl * ml.y;                                  // per lane; summed over the warp at the end
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+            const float w = __shfl_sync(0xffffffffu, wl, u);
+            if (u < cnt) {
+                if constexpr (VPL == 4) {
+                    o[0] += w * x[u].x; o[1] += w * x[u].y; o[2] += w * x[u].z; o[3] += w * x[u].w;
+                } else {
+                    o[0] += w * x[u].x; o[1] += w * x[u].y;
                 }
             }
         }
+        M = Mn;
     }
 #pragma unroll
     for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(0xffffffffu, den, mask);
@@ -786,6 +789,10 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
     p.HG = pool.num_kv_heads / p.HC;
     p.split_span = g.split_span;
     p.max_splits = (max_seq_len + g.split_span - 1) / g.split_span;
+    // split-minor partial rows; the fp8 tensor-core kernel writes head-minor ones
+    const bool fp8_tc = pool.dtype == WF_DTYPE_FP8_E4M3 && fp8_on_tensor_cores(pool, num_q_heads);
+    p.ps_h = fp8_tc ? 1 : p.max_splits;
+    p.ps_s = fp8_tc ? num_q_heads : 1;
     p.stages = 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     const int64_t rows = (int64_t)B * p.max_splits * num_q_heads;

@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(192, 1)
                     uint32_t okmask = 0;
                     for (int x = 0; x < SUB * NB; ++x) okmask |= ((okl >> (x * per_box)) & 1u) << x;
                     TcMeta m;
-                    m.b = b; m.split = split; m.nsplit = nitems / p.HGRP; m.hg = hg; m.nvalid = nvalid; m.item = k;
+                    m.b = b; m.split = split; m.nsplit = (len + kSpan - 1) / kSpan; m.hg = hg; m.nvalid = nvalid; m.item = k;
                     m.flags = (j == 0 ? 1 : 0) | (j == ntiles - 1 ? 2 : 0) | (int)(okmask << 8);
                     m.pad = 0;
                     meta[st] = m;
@@ -472,7 +472,8 @@ __global__ void __launch_bounds__(192, 1)
                 const float* Lsum = l_buf + (m.item % 3) * NCOL;
                 const float* Mx = m_buf + (m.item % 3) * NCOL;
                 const int64_t qbase = (int64_t)m.b * p.H_q + (int64_t)m.hg * NS;   // first query head of the item
-                const int64_t wrow = ((int64_t)m.b * p.max_splits + m.split) * p.H_q + (int64_t)m.hg * NS;
+                // split-minor partial rows: the item's first query head; query head qh is max_splits rows on
+                const int64_t wrow = partial_row(m.b, (int64_t)m.hg * NS, m.split, p.H_q, p.max_splits, p.max_splits, 1);
                 if constexpr (NB == 1) {
                     // one stream per query head (column qh)
 #pragma unroll
@@ -483,11 +484,11 @@ __global__ void __launch_bounds__(192, 1)
                                 static_cast<__nv_bfloat16*>(p.out)[(qbase + cc) * D + i] =
                                     __float2bfloat16_rn(acc[cc] / Lsum[cc]);
                         } else if (i < D) {
-                            p.ws_o[(wrow + cc) * D + i] = acc[cc];
+                            p.ws_o[(wrow + (int64_t)cc * p.max_splits) * D + i] = acc[cc];
                         }
                     }
                     if (m.nsplit != 1 && quad == 0 && lane < NS)
-                        p.ws_ml[wrow + lane] = make_float2(Mx[lane], Lsum[lane]);
+                        p.ws_ml[wrow + (int64_t)lane * p.max_splits] = make_float2(Mx[lane], Lsum[lane]);
                 } else {
                     // Merge the box streams: query head qh of the item owns columns
                     // qh + x * NS (x < NB).  Lane c works out the weight 2^(m_c - M_qh)
@@ -527,10 +528,10 @@ __global__ void __launch_bounds__(192, 1)
                                 static_cast<__nv_bfloat16*>(p.out)[(qbase + cc) * D + i] =
                                     __float2bfloat16_rn(acc[cc] / lq);
                         } else if (i < D) {
-                            p.ws_o[(wrow + cc) * D + i] = acc[cc];
+                            p.ws_o[(wrow + (int64_t)cc * p.max_splits) * D + i] = acc[cc];
                         }
                     }
-                    if (m.nsplit != 1 && quad == 0 && lane < NS) p.ws_ml[wrow + lane] = make_float2(m_q, l_q);
+                    if (m.nsplit != 1 && quad == 0 && lane < NS) p.ws_ml[wrow + (int64_t)lane * p.max_splits] = make_float2(m_q, l_q);
                 }
             }
         };

@@ -161,10 +161,6 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // the combine grid that follows may be scheduled now; it waits for this grid to
-    // finish before it reads anything
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
     if (warp == 1) {
         tc::alloc(tmem_slot, 128);
         tc::relinquish();
@@ -505,26 +501,46 @@ __global__ void __launch_bounds__(kThreadsFp8, 1)
                 acc[c + 2] = acc[c + 2] * a4.z + o[c + 2];
                 acc[c + 3] = acc[c + 3] * a4.w + o[c + 3];
             }
-            if (rec.last) {
-                if (rec.nsplit == 1) {
-                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (int64_t)rec.b * p.H_q * kD + i;
+            // At an item's end, everything the stores need comes out of the record
+            // first: the record is released before the global stores are issued, so
+            // the release (which orders this thread's earlier writes) does not wait
+            // for them (measured 14 us a call at the Llama-3-8B batch otherwise).
+            const bool last = rec.last;
+            const bool direct = rec.nsplit == 1;
+            const int ob = rec.b, osplit = rec.split;
+            float mi = 0.f, li = 0.f;
+            if (last) {
 #pragma unroll
-                    for (int c = 0; c < HQ; ++c)
-                        dst[c * kD] = __float2bfloat16_rn(acc[c] * p.v_head[c / G] / rec.l[c]);
-                } else {
-                    const int64_t base = ((int64_t)rec.b * p.max_splits + rec.split) * p.H_q;
-#pragma unroll
-                    for (int c = 0; c < HQ; ++c) p.ws_o[(base + c) * kD + i] = acc[c] * p.v_head[c / G];
-                    if (i < HQ) p.ws_ml[base + i] = make_float2(rec.m[i], rec.l[i]);
+                for (int c = 0; c < HQ; ++c)   // acc restarts at the next item's first tile (alpha 0)
+                    acc[c] = direct ? acc[c] * p.v_head[c / G] / rec.l[c] : acc[c] * p.v_head[c / G];
+                if (i < HQ) {
+                    mi = rec.m[i];
+                    li = rec.l[i];
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_free[rs]);
+            if (last) {
+                if (direct) {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (int64_t)ob * p.H_q * kD + i;
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c) dst[c * kD] = __float2bfloat16_rn(acc[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < HQ; ++c)   // head-minor partial rows: one split's heads are contiguous
+                        p.ws_o[partial_row(ob, c, osplit, p.H_q, p.max_splits, 1, p.H_q) * kD + i] = acc[c];
+                    if (i < HQ) p.ws_ml[partial_row(ob, i, osplit, p.H_q, p.max_splits, 1, p.H_q)] = make_float2(mi, li);
+                }
+            }
         }
     }
 
     tc::fence_before_sync();
     __syncthreads();
+    // the combine grid that follows may be scheduled now (it waits for this grid to
+    // finish before it reads anything); signalled at the end so that its CTAs take
+    // no room on the SMs while this grid streams
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 1) {
         __syncwarp();
         tc::fence_after_sync();

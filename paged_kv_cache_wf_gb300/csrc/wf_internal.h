@@ -48,6 +48,16 @@ struct DecodeGeometry {
 };
 
 bool decode_geometry(const wf_pool_desc& pool, int32_t num_q_heads, DecodeGeometry* g);
+
+// Row of the split partial (o: D floats, (m, l): one float2) of split `split` of
+// query head hq of sequence b.  Two layouts, chosen per split kernel by what its
+// writes and the combine's reads measured best: split-minor (ps_h = max_splits,
+// ps_s = 1), where the splits of one (sequence, query head) are one run of rows,
+// and head-minor (ps_h = 1, ps_s = H_q), where one split's query heads are.
+__host__ __device__ inline int64_t partial_row(int64_t b, int64_t hq, int64_t split, int64_t H_q,
+                                               int64_t max_splits, int64_t ps_h, int64_t ps_s) {
+    return b * H_q * max_splits + hq * ps_h + split * ps_s;
+}
 size_t decode_workspace_bytes(int32_t B, int32_t num_q_heads, int32_t max_seq_len,
                               const wf_pool_desc& pool);
 
