@@ -66,7 +66,8 @@ typedef enum wf_dtype {
 
 /* Bits the kernels OR into *dev_status. */
 #define WF_DEV_BAD_SLOT    0x1u  /* slot_mapping[t] >= N*P: token t not written              */
-#define WF_DEV_BAD_BLOCK   0x2u  /* block id outside [0, N): that block's rows were skipped  */
+#define WF_DEV_BAD_BLOCK   0x2u  /* block id outside [0, N): that block's rows were skipped
+                                    (fp8 pools at D = 64: the 32 positions of its tile)       */
 #define WF_DEV_BAD_SEQLEN  0x4u  /* seq_lens[b] < 1, > max_seq_len, > M*P, or < q_len:
                                     sequence b was skipped and its output left unwritten    */
 #define WF_DEV_TIMEOUT     0x8u  /* a wait gave up: an internal pipeline wait (should never

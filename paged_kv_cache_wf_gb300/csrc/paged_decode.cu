@@ -829,7 +829,8 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
                                                      seq_lens, B, max_seq_len, num_q_heads, scale, pool, p.ws_o,
                                                      p.ws_ml, p.max_splits, queue, prep, dev_status, stream);
         if (err != cudaSuccess) return err;
-        return p.max_splits > 1 ? launch_combine<BF16, 128>(p, stream) : cudaSuccess;
+        if (p.max_splits <= 1) return cudaSuccess;
+        return pool.head_dim == 64 ? launch_combine<BF16, 64>(p, stream) : launch_combine<BF16, 128>(p, stream);
     }
     if (pool.dtype == WF_DTYPE_F32) {
         return pool.head_dim == 64 ? launch_group<F32, 64>(p, g.gmax, stream)

@@ -49,7 +49,7 @@ cudaError_t encode_tiled_bf16(CUtensorMap* map, void* base, int rank, const uint
 }
 
 cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, void* base, int rank, const uint64_t* dims,
-                         const uint64_t* strides, const uint32_t* box) {
+                         const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle) {
     static std::mutex mu;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     {
@@ -72,7 +72,7 @@ cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, void* base,
         if (i + 1 < rank) s[i] = strides[i];
     }
     const CUresult r = fn(map, type, (cuuint32_t)rank, base, d, s, bx, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

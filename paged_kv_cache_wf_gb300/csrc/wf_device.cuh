@@ -435,6 +435,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
     return d;
 }
 
+// The same for a 64-byte-swizzled tile (8-row x 64-byte atoms, 512-byte aligned).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
+    d |= (uint64_t)4 << 61;   // swizzle: 64 bytes
+    return d;
+}
+
 // Thread t of warp w reads TMEM lane 32*(w%4) + t%32, 32 consecutive fp32 columns.
 __device__ __forceinline__ void ld_32cols(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];

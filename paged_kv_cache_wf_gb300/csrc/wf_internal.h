@@ -25,7 +25,8 @@ cudaError_t allow_dynamic_smem(const void* kernel, int bytes);
 cudaError_t encode_tiled_bf16(CUtensorMap* map, void* base, int rank, const uint64_t* dims,
                               const uint64_t* strides, const uint32_t* box);
 cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType type, void* base, int rank, const uint64_t* dims,
-                         const uint64_t* strides, const uint32_t* box);
+                         const uint64_t* strides, const uint32_t* box,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                      const int64_t* slot_mapping, int32_t num_tokens,

@@ -112,7 +112,9 @@ CASES = {
     # shapes the tensor-core kernel does not take: the CUDA-core kernel widens the codes
     "core_mha12_D64": lambda: W.custom_layout(12, 12, 64, 16, W.BF16, [700, 1, 256, 63, 65], seed=25),
     "core_gqa8_D128_P7": lambda: W.custom_layout(16, 2, 128, 7, W.BF16, [300, 1, 129, 128, 127], seed=26),
-    "core_gqa4_D64": lambda: W.custom_layout(32, 8, 64, 16, W.BF16, [1, 15, 257, 2049], seed=27),
+    # D = 64: two 16-position sub-tiles of 64-byte code rows per stage
+    "gqa4_D64": lambda: W.custom_layout(32, 8, 64, 16, W.BF16, [1, 15, 16, 17, 31, 32, 33, 257, 2049], seed=27),
+    "gqa2_D64_P32": lambda: W.custom_layout(16, 8, 64, 32, W.BF16, [2, 33, 64, 300, 1000], seed=32),
     # one long context in 64-slot blocks (many splits: combine path)
     "gqa4_long_P64": lambda: W.custom_layout(32, 8, 128, 64, W.BF16, [5000, 33, 128], seed=23),
 }
@@ -286,7 +288,7 @@ def test_fp8_per_head_scatter_bit_exact():
     assert wf.wf_device_status_fetch(st) == 0
 
 
-@pytest.mark.parametrize("name", ["gqa4_ragged", "gqa2_P32", "core_mha12_D64", "core_gqa4_D64"])
+@pytest.mark.parametrize("name", ["gqa4_ragged", "gqa2_P32", "core_mha12_D64", "gqa4_D64"])
 def test_fp8_per_head_decode_matches_oracle(name):
     torch = G.torch_mod()
     lay = CASES[name]()
