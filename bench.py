@@ -489,6 +489,39 @@ class MixedWorkload:
         for l in range(self.L):
             self.layer(l, evs.pop() if evs is not None else None)
 
+    def step_one_call(self):
+        """The step with each layer's prefill and decode in one wf_paged_prefill_decode
+        call (one grid when the shapes allow it)."""
+        g = self.pf.geom
+        for l in range(self.L):
+            kp, vp = self.pools[l]
+            rc = self.lib.wf_reshape_and_cache(self.knew[l].data_ptr(), self.vnew[l].data_ptr(), kp.data_ptr(),
+                                               vp.data_ptr(), self.slots.data_ptr(), int(self.slots.shape[0]),
+                                               self.desc, self.status.data_ptr(), self.sp)
+            assert rc == 0, rc
+            pq, dq = self.pvals[l][0], self.dvals[l][0]
+            rc = self.lib.wf_paged_prefill_decode(
+                self.pouts[l].data_ptr(), pq.data_ptr(), self.pbt.data_ptr(), int(self.pbt.shape[1]),
+                self.psl.data_ptr(), self.pcu.data_ptr(), self.pf.B, int(pq.shape[0]), self.pf.max_q_len,
+                self.pf.max_seq_len, self.douts[l].data_ptr(), dq.data_ptr(), self.dbt.data_ptr(),
+                int(self.dbt.shape[1]), self.dsl.data_ptr(), self.dc.B, self.dc.max_seq_len, kp.data_ptr(),
+                vp.data_ptr(), g.H_q, self.scale, self.desc, self.ws.data_ptr(), self.ws_bytes,
+                self.status.data_ptr(), self.sp)
+            assert rc == 0, rc
+
+    def timed_one_call(self, steps: int) -> float:
+        torch = self.torch
+        for _ in range(2):
+            self.step_one_call()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.synchronize()
+        ev[0].record(self.stream)
+        for _ in range(steps):
+            self.step_one_call()
+        ev[1].record(self.stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1])
+
     def step_two_streams(self, side):
         """The step with each layer's decode on a second stream beside its prefill
         (both read the pool after the layer's scatter and are independent), as an
@@ -619,6 +652,9 @@ def run_mixed(args, rank, world):
     two_ms = wl.timed_two_streams(args.steps) / args.steps
     if wl.wf.wf_device_status_fetch(wl.status) != 0:
         raise SystemExit("device status flagged an error during the two-stream steps")
+    one_ms = wl.timed_one_call(args.steps) / args.steps
+    if wl.wf.wf_device_status_fetch(wl.status) != 0:
+        raise SystemExit("device status flagged an error during the one-call steps")
     peaks, src = load_peaks()
     ms_step = total_ms / args.steps
     flops = prefill_flops(pf)
@@ -650,6 +686,11 @@ def run_mixed(args, rank, world):
         "two_streams": {"value": world * tok * L / (two_ms / 1e3), "unit": "tokens·layers/s", "ms_per_step": two_ms,
                         "note": "each layer's decode on a second stream beside its prefill, timed separately "
                                 "after the main run; the kernel rooflines above come from the sequential run"},
+        "one_call": {"value": world * tok * L / (one_ms / 1e3), "unit": "tokens·layers/s", "ms_per_step": one_ms,
+                     "fused": bool(wl.wf.wf_paged_prefill_decode_fused(wl.desc, g.H_q)),
+                     "note": "each layer's prefill and decode in one wf_paged_prefill_decode call (one grid: "
+                             "prefill CTAs first, then persistent decode CTAs that fill the SMs the prefill's "
+                             "tail leaves idle), timed separately after the main run"},
         "clocks": clk,
     }
     if rank == 0:

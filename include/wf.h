@@ -204,6 +204,36 @@ wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const v
                            uint32_t* dev_status, cudaStream_t stream);
 
 /*
+ * wf_paged_prefill_decode -- the attention of a mixed continuous-batching step:
+ * wf_paged_prefill of the step's new requests and wf_paged_decode of its running
+ * sequences, over one pool, in one call.
+ * (tiny-vllm-py, "Inference Server Flow": a step mixes prefill and decode work;
+ *  ember, "Deliberately out of scope": a proper prefill/decode mix per step)
+ *
+ * The pf_* arguments are those of wf_paged_prefill, the dec_* ones those of
+ * wf_paged_decode (its workspace too), and both share the pools, num_q_heads,
+ * scale and pool descriptor; every rule of the two calls applies.  The outputs
+ * are those of the two calls (the prefill and the decode outputs must not
+ * overlap).  For bf16 pools whose prefill and decode both run on the tensor cores,
+ * H_kv a multiple of 8 and GQA groups of 1, 2 or 4, both run in one grid: its first
+ * CTAs are the prefill's, the rest are persistent decode CTAs that take decode
+ * work from a queue as the prefill's CTAs finish, so the decode fills the SMs the
+ * prefill's tail leaves idle.  Other shapes run the two calls one after the other.
+ */
+wf_status wf_paged_prefill_decode(void* pf_out, const void* pf_q, const int32_t* pf_block_tables,
+                                  int32_t pf_max_blocks_per_seq, const int32_t* pf_seq_lens,
+                                  const int32_t* cu_q_lens, int32_t pf_B, int32_t total_q, int32_t max_q_len,
+                                  int32_t pf_max_seq_len, void* dec_out, const void* dec_q,
+                                  const int32_t* dec_block_tables, int32_t dec_max_blocks_per_seq,
+                                  const int32_t* dec_seq_lens, int32_t dec_B, int32_t dec_max_seq_len,
+                                  const void* k_pool, const void* v_pool, int32_t num_q_heads, float scale,
+                                  wf_pool_desc pool, void* workspace, size_t workspace_bytes,
+                                  uint32_t* dev_status, cudaStream_t stream);
+/* 1 when wf_paged_prefill_decode runs both in one grid for this geometry, else 0
+ * (host-only, no CUDA call). */
+int wf_paged_prefill_decode_fused(wf_pool_desc pool, int32_t num_q_heads);
+
+/*
  * Size of the fixed device array wf_paged_decode_static_scratch uses as its
  * workspace (32 MiB).  A device holds it from the first
  * wf_paged_decode_static_scratch call on that device until the process exits.

@@ -26,6 +26,8 @@ EXPORTS = (
     "wf_paged_decode_workspace_size",
     "wf_paged_decode",
     "wf_paged_prefill",
+    "wf_paged_prefill_decode",
+    "wf_paged_prefill_decode_fused",
     "wf_paged_decode_static_scratch",
     "wf_decode_worker",
     "wf_paged_decode_kernel",
@@ -84,6 +86,11 @@ def load(path: str = LIB_PATH):
         lib.wf_paged_prefill.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, f32,
                                          wf_pool_desc, vp, vp]
         lib.wf_paged_prefill.restype = ctypes.c_int
+        lib.wf_paged_prefill_decode.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, i32,
+                                                i32, vp, vp, i32, f32, wf_pool_desc, vp, sz, vp, vp]
+        lib.wf_paged_prefill_decode.restype = ctypes.c_int
+        lib.wf_paged_prefill_decode_fused.argtypes = [wf_pool_desc, i32]
+        lib.wf_paged_prefill_decode_fused.restype = ctypes.c_int
         lib.wf_paged_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, f32,
                                                        wf_pool_desc, vp, vp]
         lib.wf_paged_decode_static_scratch.restype = ctypes.c_int
@@ -245,6 +252,29 @@ def wf_paged_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens, 
                               int(max_q_len), int(max_seq_len), int(H_q), float(scale),
                               pool_desc(k_pool), _ptr(dev_status), _stream(stream))
     _check("wf_paged_prefill", rc)
+
+
+def wf_paged_prefill_decode_fused(desc: wf_pool_desc, num_q_heads: int) -> bool:
+    """Whether wf_paged_prefill_decode runs the step in one grid for this geometry."""
+    return bool(load().wf_paged_prefill_decode_fused(desc, int(num_q_heads)))
+
+
+def wf_paged_prefill_decode(pf_out, pf_q, pf_block_tables, pf_seq_lens, cu_q_lens, max_q_len: int,
+                            pf_max_seq_len: int, dec_out, dec_q, dec_block_tables, dec_seq_lens, dec_max_seq_len: int,
+                            k_pool, v_pool, scale: float, workspace, dev_status=None, stream=None):
+    """The step's prefill (as wf_paged_prefill) and decode (as wf_paged_decode) in one call."""
+    _contig(pf_out, pf_q, pf_block_tables, pf_seq_lens, cu_q_lens, dec_out, dec_q, dec_block_tables, dec_seq_lens,
+            k_pool, v_pool)
+    lib = load()
+    T, H_q, _ = pf_q.shape
+    rc = lib.wf_paged_prefill_decode(
+        _ptr(pf_out), _ptr(pf_q), _ptr(pf_block_tables), int(pf_block_tables.shape[1]), _ptr(pf_seq_lens),
+        _ptr(cu_q_lens), int(pf_seq_lens.shape[0]), int(T), int(max_q_len), int(pf_max_seq_len), _ptr(dec_out),
+        _ptr(dec_q), _ptr(dec_block_tables), int(dec_block_tables.shape[1]), _ptr(dec_seq_lens),
+        int(dec_q.shape[0]), int(dec_max_seq_len), _ptr(k_pool), _ptr(v_pool), int(H_q), float(scale),
+        pool_desc(k_pool), _ptr(workspace), int(workspace.numel() * workspace.element_size()), _ptr(dev_status),
+        _stream(stream))
+    _check("wf_paged_prefill_decode", rc)
 
 
 WF_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024

@@ -762,14 +762,14 @@ size_t decode_workspace_bytes(int32_t B, int32_t num_q_heads, int32_t max_seq_le
     return (size_t)base;
 }
 
-cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
-                                int32_t num_q_heads, float scale, const wf_pool_desc& pool,
-                                void* workspace, uint32_t* dev_status, cudaStream_t stream) {
-    DecodeGeometry g;
-    if (!decode_geometry(pool, num_q_heads, &g)) return cudaErrorInvalidValue;
-    DecodeParams p;
+// The decode's parameters, with the workspace carved into split partials and the
+// tensor-core kernels' work-item queue.
+static bool decode_setup(void* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t B,
+                         int32_t max_seq_len, int32_t num_q_heads, float scale, const wf_pool_desc& pool,
+                         void* workspace, uint32_t* dev_status, DecodeGeometry& g, DecodeParams& p,
+                         uint32_t*& queue) {
+    if (!decode_geometry(pool, num_q_heads, &g)) return false;
     p.out = out;
     p.q = q;
     p.k_pool = static_cast<const char*>(k_pool);
@@ -799,11 +799,27 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
     const int64_t o_bytes = ((rows * pool.head_dim * 4 + 255) / 256) * 256;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
-    const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
     // the tensor-core kernels' work-item queue: one word after the (m, l) partials,
     // inside the workspace's slack, zeroed by a small grid that runs before each
     // decode grid (for fp8 pools, the grid that prepares q)
-    uint32_t* queue = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + o_bytes + (rows * 8 + 15) / 16 * 16);
+    queue = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + o_bytes + (rows * 8 + 15) / 16 * 16);
+    return true;
+}
+
+cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                                int32_t num_q_heads, float scale, const wf_pool_desc& pool,
+                                void* workspace, uint32_t* dev_status, cudaStream_t stream) {
+    DecodeGeometry g;
+    DecodeParams p;
+    uint32_t* queue = nullptr;
+    if (!decode_setup(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B, max_seq_len, num_q_heads,
+                      scale, pool, workspace, dev_status, g, p, queue))
+        return cudaErrorInvalidValue;
+    const int64_t rows = (int64_t)B * p.max_splits * num_q_heads;
+    const int64_t o_bytes = ((rows * pool.head_dim * 4 + 255) / 256) * 256;
+    const int64_t slots = (int64_t)pool.num_blocks * pool.block_size;
     if (decode_tc_supported(pool, num_q_heads) && slots <= INT32_MAX) {
         cudaError_t err = launch_paged_decode_tc(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B,
                                      max_seq_len, num_q_heads, scale, pool, p.ws_o, p.ws_ml, p.max_splits, queue,
@@ -838,6 +854,47 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* k_pool, co
     }
     return pool.head_dim == 64 ? launch_group<BF16, 64>(p, g.gmax, stream)
                                : launch_group<BF16, 128>(p, g.gmax, stream);
+}
+
+cudaError_t launch_paged_prefill_decode(void* pf_out, const void* pf_q, const int32_t* pf_block_tables,
+                                       int32_t pf_max_blocks_per_seq, const int32_t* pf_seq_lens,
+                                       const int32_t* cu_q_lens, int32_t pf_B, int32_t total_q, int32_t max_q_len,
+                                       int32_t pf_max_seq_len, void* dec_out, const void* dec_q,
+                                       const int32_t* dec_block_tables, int32_t dec_max_blocks_per_seq,
+                                       const int32_t* dec_seq_lens, int32_t dec_B, int32_t dec_max_seq_len,
+                                       const void* k_pool, const void* v_pool, int32_t num_q_heads, float scale,
+                                       const wf_pool_desc& pool, void* workspace, uint32_t* dev_status,
+                                       cudaStream_t stream) {
+    const bool has_pf = pf_B > 0 && total_q > 0 && max_q_len > 0;
+    if (!has_pf || dec_B == 0 || !mixed_tc_supported(pool, num_q_heads)) {
+        // nothing to share a launch, or shapes the one-launch kernel does not take:
+        // the two calls one after the other
+        if (has_pf) {
+            cudaError_t err = launch_paged_prefill(pf_out, pf_q, k_pool, v_pool, pf_block_tables,
+                                                   pf_max_blocks_per_seq, pf_seq_lens, cu_q_lens, pf_B, total_q,
+                                                   max_q_len, pf_max_seq_len, num_q_heads, scale, pool, dev_status,
+                                                   stream);
+            if (err != cudaSuccess) return err;
+        }
+        if (dec_B == 0) return cudaSuccess;
+        return launch_paged_decode(dec_out, dec_q, k_pool, v_pool, dec_block_tables, dec_max_blocks_per_seq,
+                                   dec_seq_lens, dec_B, dec_max_seq_len, num_q_heads, scale, pool, workspace,
+                                   dev_status, stream);
+    }
+    DecodeGeometry g;
+    DecodeParams p;
+    uint32_t* queue = nullptr;
+    if (!decode_setup(dec_out, dec_q, k_pool, v_pool, dec_block_tables, dec_max_blocks_per_seq, dec_seq_lens, dec_B,
+                      dec_max_seq_len, num_q_heads, scale, pool, workspace, dev_status, g, p, queue))
+        return cudaErrorInvalidValue;
+    cudaError_t err = launch_paged_mixed_tc(pf_out, pf_q, pf_block_tables, pf_max_blocks_per_seq, pf_seq_lens,
+                                            cu_q_lens, pf_B, total_q, max_q_len, pf_max_seq_len, dec_out, dec_q,
+                                            dec_block_tables, dec_max_blocks_per_seq, dec_seq_lens, dec_B,
+                                            dec_max_seq_len, k_pool, v_pool, num_q_heads, scale, pool, p.ws_o,
+                                            p.ws_ml, p.max_splits, queue, dev_status, stream);
+    if (err != cudaSuccess) return err;
+    if (p.max_splits <= 1) return cudaSuccess;
+    return pool.head_dim == 64 ? launch_combine<BF16, 64>(p, stream) : launch_combine<BF16, 128>(p, stream);
 }
 
 }  // namespace wf

@@ -163,12 +163,16 @@ size_t wf_paged_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t ma
     return wf::decode_workspace_bytes(B, num_q_heads, max_seq_len, pool);
 }
 
-wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
-                          const int32_t* block_tables, int32_t max_blocks_per_seq,
-                          const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
-                          int32_t num_q_heads, float scale, wf_pool_desc pool,
-                          void* workspace, size_t workspace_bytes, uint32_t* dev_status,
-                          cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// wf_paged_decode's argument rules (WF_OK also for an empty batch, which launches
+// nothing).
+wf_status decode_args(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                      int32_t num_q_heads, float scale, const wf_pool_desc& pool, void* workspace,
+                      size_t workspace_bytes) {
     wf_status s = check_pool(pool);
     if (s != WF_OK) return s;
     if (B < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 1) return WF_ERR_INVALID_ARG;
@@ -184,17 +188,36 @@ wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const vo
     const size_t need = wf::decode_workspace_bytes(B, num_q_heads, max_seq_len, pool);
     if (need == 0) return WF_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return WF_ERR_WORKSPACE;
+    return WF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                          int32_t num_q_heads, float scale, wf_pool_desc pool,
+                          void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                          cudaStream_t stream) {
+    const wf_status s = decode_args(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, B,
+                                    max_seq_len, num_q_heads, scale, pool, workspace, workspace_bytes);
+    if (s != WF_OK || B == 0) return s;
     return from_cuda(wf::launch_paged_decode(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
                                              seq_lens, B, max_seq_len, num_q_heads, scale, pool,
                                              workspace, dev_status, stream));
 }
 
-wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
-                           const int32_t* block_tables, int32_t max_blocks_per_seq,
-                           const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
-                           int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
-                           int32_t num_q_heads, float scale, wf_pool_desc pool,
-                           uint32_t* dev_status, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// wf_paged_prefill's argument rules (WF_OK also for calls that launch nothing).
+wf_status prefill_args(void* out, const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* cu_q_lens, int32_t B, int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
+                       int32_t num_q_heads, float scale, const wf_pool_desc& pool) {
     wf_status s = check_pool(pool);
     if (s != WF_OK) return s;
     if (pool.dtype != WF_DTYPE_BF16) return WF_ERR_UNSUPPORTED;
@@ -212,9 +235,50 @@ wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const v
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
         (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u))
         return WF_ERR_INVALID_ARG;
+    return WF_OK;
+}
+
+bool prefill_launches(int32_t B, int32_t total_q, int32_t max_q_len) { return B > 0 && total_q > 0 && max_q_len > 0; }
+
+}  // namespace
+
+extern "C" {
+
+wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
+                           int32_t total_q, int32_t max_q_len, int32_t max_seq_len,
+                           int32_t num_q_heads, float scale, wf_pool_desc pool,
+                           uint32_t* dev_status, cudaStream_t stream) {
+    const wf_status s = prefill_args(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens,
+                                     B, total_q, max_q_len, max_seq_len, num_q_heads, scale, pool);
+    if (s != WF_OK || !prefill_launches(B, total_q, max_q_len)) return s;
     return from_cuda(wf::launch_paged_prefill(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
                                               seq_lens, cu_q_lens, B, total_q, max_q_len, max_seq_len,
                                               num_q_heads, scale, pool, dev_status, stream));
+}
+
+wf_status wf_paged_prefill_decode(void* pf_out, const void* pf_q, const int32_t* pf_block_tables,
+                                  int32_t pf_max_blocks_per_seq, const int32_t* pf_seq_lens,
+                                  const int32_t* cu_q_lens, int32_t pf_B, int32_t total_q, int32_t max_q_len,
+                                  int32_t pf_max_seq_len, void* dec_out, const void* dec_q,
+                                  const int32_t* dec_block_tables, int32_t dec_max_blocks_per_seq,
+                                  const int32_t* dec_seq_lens, int32_t dec_B, int32_t dec_max_seq_len,
+                                  const void* k_pool, const void* v_pool, int32_t num_q_heads, float scale,
+                                  wf_pool_desc pool, void* workspace, size_t workspace_bytes,
+                                  uint32_t* dev_status, cudaStream_t stream) {
+    wf_status s = prefill_args(pf_out, pf_q, k_pool, v_pool, pf_block_tables, pf_max_blocks_per_seq, pf_seq_lens,
+                               cu_q_lens, pf_B, total_q, max_q_len, pf_max_seq_len, num_q_heads, scale, pool);
+    if (s != WF_OK) return s;
+    s = decode_args(dec_out, dec_q, k_pool, v_pool, dec_block_tables, dec_max_blocks_per_seq, dec_seq_lens, dec_B,
+                    dec_max_seq_len, num_q_heads, scale, pool, workspace, workspace_bytes);
+    if (s != WF_OK) return s;
+    const bool pf = prefill_launches(pf_B, total_q, max_q_len);
+    if (!pf && dec_B == 0) return WF_OK;
+    return from_cuda(wf::launch_paged_prefill_decode(
+        pf_out, pf_q, pf_block_tables, pf_max_blocks_per_seq, pf_seq_lens, cu_q_lens, pf ? pf_B : 0, total_q,
+        max_q_len, pf_max_seq_len, dec_out, dec_q, dec_block_tables, dec_max_blocks_per_seq, dec_seq_lens, dec_B,
+        dec_max_seq_len, k_pool, v_pool, num_q_heads, scale, pool, workspace, dev_status, stream));
 }
 
 wf_status wf_decode_worker(void* out, const void* q, int32_t num_rows, const void* k_pool, const void* v_pool,
@@ -240,6 +304,11 @@ wf_status wf_decode_worker(void* out, const void* q, int32_t num_rows, const voi
     return from_cuda(wf::launch_decode_worker(out, q, num_rows, k_pool, v_pool, block_tables, num_table_rows,
                                               max_blocks_per_seq, num_q_heads, scale, pool, tasks, task_capacity,
                                               mailbox, num_workers, idle_timeout_ns, dev_status, stream));
+}
+
+int wf_paged_prefill_decode_fused(wf_pool_desc pool, int32_t num_q_heads) {
+    if (check_pool(pool) != WF_OK || num_q_heads < 1) return 0;
+    return wf::mixed_tc_supported(pool, num_q_heads) ? 1 : 0;
 }
 
 int wf_paged_decode_kernel(wf_pool_desc pool, int32_t num_q_heads) {

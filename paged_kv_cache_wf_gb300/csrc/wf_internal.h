@@ -118,6 +118,31 @@ cudaError_t launch_decode_worker(void* out, const void* q, int32_t num_rows, con
                                  int32_t num_workers, uint64_t idle_timeout_ns, uint32_t* dev_status,
                                  cudaStream_t stream);
 
+// ---- mixed step (paged_mixed_tc.cu) -------------------------------------------
+// One launch for a step's prefill and decode over one pool: bf16, both tensor-core
+// kernels, H_kv a multiple of 8, groups of 1, 2 or 4.
+bool mixed_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads);
+cudaError_t launch_paged_mixed_tc(void* pf_out, const void* pf_q, const int32_t* pf_block_tables,
+                                  int32_t pf_max_blocks_per_seq, const int32_t* pf_seq_lens, const int32_t* cu_q_lens,
+                                  int32_t pf_B, int32_t total_q, int32_t max_q_len, int32_t pf_max_seq_len,
+                                  void* dec_out, const void* dec_q, const int32_t* dec_block_tables,
+                                  int32_t dec_max_blocks_per_seq, const int32_t* dec_seq_lens, int32_t dec_B,
+                                  int32_t dec_max_seq_len, const void* k_pool, const void* v_pool,
+                                  int32_t num_q_heads, float scale, const wf_pool_desc& pool, float* ws_o,
+                                  float2* ws_ml, int32_t max_splits, uint32_t* queue, uint32_t* dev_status,
+                                  cudaStream_t stream);
+// The step's prefill and decode: one launch when mixed_tc_supported, else the two
+// calls one after the other (paged_decode.cu).
+cudaError_t launch_paged_prefill_decode(void* pf_out, const void* pf_q, const int32_t* pf_block_tables,
+                                       int32_t pf_max_blocks_per_seq, const int32_t* pf_seq_lens,
+                                       const int32_t* cu_q_lens, int32_t pf_B, int32_t total_q, int32_t max_q_len,
+                                       int32_t pf_max_seq_len, void* dec_out, const void* dec_q,
+                                       const int32_t* dec_block_tables, int32_t dec_max_blocks_per_seq,
+                                       const int32_t* dec_seq_lens, int32_t dec_B, int32_t dec_max_seq_len,
+                                       const void* k_pool, const void* v_pool, int32_t num_q_heads, float scale,
+                                       const wf_pool_desc& pool, void* workspace, uint32_t* dev_status,
+                                       cudaStream_t stream);
+
 // ---- prefill ------------------------------------------------------------------
 // Pipelined tcgen05 prefill (bf16, P % 16 == 0, G in {1, 2, 4, 8}, D in {64, 128}).
 bool prefill_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads);

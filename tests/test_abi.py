@@ -247,3 +247,22 @@ def test_decode_worker_argument_checks(lib):
     assert call(ok(scale=float("inf"))) == wf.WF_ERR_INVALID_ARG
     assert call(ok(pool=_fp8(N=10, P=16, H=2, D=64))) == wf.WF_ERR_UNSUPPORTED
     assert call(ok(tasks=None)) == wf.WF_ERR_INVALID_ARG
+
+
+def test_prefill_decode_query_and_argument_checks(lib):
+    d = _desc(N=100, P=16, H=8, D=128)
+    assert lib.wf_paged_prefill_decode_fused(d, 32) == 1          # Llama-3-8B heads: one grid
+    assert lib.wf_paged_prefill_decode_fused(d, 64) == 0          # a group of 8: two launches
+    assert lib.wf_paged_prefill_decode_fused(_desc(N=100, P=16, H=2, D=128), 8) == 0   # H_kv not a multiple of 8
+    assert lib.wf_paged_prefill_decode_fused(_desc(N=100, P=7, H=8, D=128), 32) == 0   # P % 16 != 0
+    f = lib.wf_paged_prefill_decode
+    F = FAKE
+    ok = (F, F, F, 4, F, F, 2, 10, 8, 64, F, F, F, 4, F, 3, 64, F, F, 32, 0.088, d, None, 0, None, None)
+    assert f(*ok) == wf.WF_ERR_WORKSPACE                          # a decode batch needs its workspace
+    bad = list(ok); bad[20] = float("nan")
+    assert f(*bad) == wf.WF_ERR_INVALID_ARG
+    bad = list(ok); bad[9] = 4                                    # prefill max_seq_len < max_q_len
+    assert f(*bad) == wf.WF_ERR_INVALID_ARG
+    none = (None, None, None, 1, None, None, 0, 0, 0, 16, None, None, None, 1, None, 0, 16, None, None, 32, 0.088, d,
+            None, 0, None, None)
+    assert f(*none) == wf.WF_OK                                   # nothing to do
