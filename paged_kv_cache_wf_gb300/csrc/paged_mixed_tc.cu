@@ -15,7 +15,9 @@
 //
 // CTAs are dispatched in index order as SMs free up, so the decode CTAs start on
 // the SMs the prefill's tail leaves idle and take decode items from one queue until
-// it is empty: no SM is set aside for either kind of work.  The block has the
+// it is empty: no SM is set aside for either kind of work.  (The standalone prefill
+// runs as a persistent grid whose CTAs finish together; here the one-CTA-per-block
+// grid's ragged end is what the decode fills, and it measured 1.1% faster a step.)  The block has the
 // prefill's 12 warps; a decode CTA runs on its first 6 (the others leave at once,
 // and the decode's block-wide barriers are named barriers over those 6 warps).
 // Both programs only read the pool, and they write disjoint outputs, so the result

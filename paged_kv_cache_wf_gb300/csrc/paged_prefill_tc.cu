@@ -1,6 +1,7 @@
-// paged_prefill_tc.cu -- launchers of the pipelined tensor-core prefill (the kernel
-// body and its design notes are in paged_prefill_tc.cuh).
-#include "paged_prefill_tc.cuh"
+// paged_prefill_tc.cu -- launchers of the pipelined tensor-core prefill: the
+// persistent grid (paged_prefill_persist.cuh) when the batch is within its list
+// build's limits, else one CTA per query block (paged_prefill_tc.cuh).
+#include "paged_prefill_persist.cuh"
 
 namespace wf {
 
@@ -15,8 +16,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_prefill_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                                 const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    prefill_tc_persist<D, G>(tm_q, tm_k, tm_v, p, smem_raw, (int)blockIdx.x, (int)gridDim.x);
+}
+
+template <int D, int G>
 cudaError_t launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, PfParams p,
                       cudaStream_t stream) {
+    const int pgrid = prefill_persist_grid<D, G>(p.B, p.max_q_len, p.H_kv, num_sms());
+    if (pgrid > 0) {
+        const int smem = PpLayout<D, G>::total + 1024;
+        auto kern = paged_prefill_persist_kernel<D, G>;
+        cudaError_t err = allow_dynamic_smem((const void*)kern, smem);
+        if (err != cudaSuccess) return err;
+        kern<<<pgrid, kThreads, smem, stream>>>(tq, tk, tv, p);
+        return cudaGetLastError();
+    }
     using L = PfLayout<D, G>;
     p.nqblk = (p.max_q_len + L::BMQ - 1) / L::BMQ;
     const int smem = L::total + 1024;

@@ -15,8 +15,8 @@
 //               lane r: causal mask (only on tiles that cross the diagonal), online
 //               softmax in the exp2 domain with a lazy rescale (O in TMEM is rescaled
 //               only when a row max grows by more than 2^8), P written as bf16 pairs
-//               over the first half of the tile's S columns in TMEM; the epilogue
-//               divides O by the row sum.
+//               over S columns already read (keys 0-63 into columns 0-31, keys 64-127
+//               into columns 64-95); the epilogue divides O by the row sum.
 //   warps 8-10  producers: TMA loads of the two Q tiles (3D box d x head x token) and,
 //               tile by tile, of 128 keys of K and V gathered 16-key block by block
 //               through the block table (one box per lane, 128-byte swizzle) into a
@@ -50,6 +50,7 @@ constexpr int kThreads = (kMma + 1) * 32;
 
 struct PfParams {
     __nv_bfloat16* out;
+    const __nv_bfloat16* v_pool;   // rows of a V tile's last partial block are copied by hand
     const int32_t* block_tables;
     const int32_t* seq_lens;
     const int32_t* cu_q_lens;
@@ -91,7 +92,8 @@ struct PfLayout {
     static constexpr int tmem_slot = bars + nbars * 8;
     static constexpr int total = tmem_slot + 16;
     // TMEM: S of query tile t in columns [128 t, 128 t + 128) -- its softmax weights
-    // P (bf16 pairs) replace the first 64 of them -- and O of tile t at 256 + D t.
+    // P (bf16 pairs) replace columns 0-31 (keys 0-63) and 64-95 (keys 64-127) of
+    // them -- and O of tile t at 256 + D t.
     static constexpr int SCOL = 128;
     static constexpr int OCOL = 256;
     static constexpr int TMEM_COLS = 512;
@@ -312,7 +314,8 @@ __device__ __forceinline__ void prefill_tc_body(const CUtensorMap& tm_q, const C
                         if (lane == 0) {
 #pragma unroll
                             for (int kk = 0; kk < PN / 16; ++kk)
-                                tc::mma_f16_tmem_a(dO, pcol + kk * 8, vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
+                                tc::mma_f16_tmem_a(dO, pcol + kk * 8 + (kk >= 4 ? 32 : 0),
+                                                   vd + (uint64_t)((kk * 2 * L::ATOM) >> 4), idO,
                                                    (u > 0 || kk > 0) ? 1u : 0u);
                             tc::commit(pv_done(t));
                             if (sp[o] > u || u >= nt_t[o]) tc::commit(&slot_empty[vu % L::NSLOT]);
@@ -383,16 +386,15 @@ __device__ __forceinline__ void prefill_tc_body(const CUtensorMap& tm_q, const C
                 break;
             }
             tc::fence_after_sync();
-            // keys some row of the tile may not see are masked.  The row max is taken on
-            // raw scores (scale > 0) and scaled once.  Two passes over S in 64-column
-            // halves: the maximum, then the weights.
+            // keys some row of the tile may not see are masked.  Three round trips to
+            // TMEM: keys 0-63 (their maximum), keys 64-127 (kept in registers for their
+            // weights), keys 0-63 again.  The row max is taken on raw scores (scale > 0)
+            // and scaled once.
             const bool masked = (k0 + PN - 1 > first_key_t) || !row_valid;
             float m8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float s[2][32];
+            auto load_half = [&](int hh, float (&s)[2][32]) {
                 tc::ld_32cols(sbase + hh * 64, s[0]);
                 tc::ld_32cols(sbase + hh * 64 + 32, s[1]);
                 tc::wait_ld();
@@ -405,12 +407,18 @@ __device__ __forceinline__ void prefill_tc_body(const CUtensorMap& tm_q, const C
                             s[c2][e] = vis ? s[c2][e] : -INFINITY;
                         }
                 }
-                // 8 independent running maxima (short dependency chains), two inputs a step
+            };
+            float s[2][32];
+            load_half(0, s);
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2)
+            for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) m8[e & 7] = fmax3(m8[e & 7], s[c2][e], s[c2][e + 16]);
-            }
+                for (int e = 0; e < 16; ++e) m8[e & 7] = fmax3(m8[e & 7], s[c2][e], s[c2][e + 16]);
+            load_half(1, s);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) m8[e & 7] = fmax3(m8[e & 7], s[c2][e], s[c2][e + 16]);
             const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                      fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float mt = mraw * p.scale_log2;
@@ -443,34 +451,26 @@ __device__ __forceinline__ void prefill_tc_body(const CUtensorMap& tm_q, const C
             const float2 nm2 = make_float2(-m_use, -m_use);
             float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pw[32];  // keys 2k, 2k+1 of this half as a bf16 pair
+            // weights of the half in registers -> bf16 pairs -> TMEM (keys 64-127 into
+            // columns 64-95, keys 0-63 into columns 0-31: S there is consumed)
+            auto weights = [&](int hh) {
+                uint32_t pw[32];
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
-                    float s[32];
-                    tc::ld_32cols(sbase + hh * 64 + c2 * 32, s);
-                    tc::wait_ld();
-                    if (masked) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const bool vis = row_valid && k0 + hh * 64 + c2 * 32 + e <= last_key;
-                            s[e] = vis ? s[e] : -INFINITY;
-                        }
-                    }
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         // exponent = s * scale*log2(e) - m_ref, two keys per fp32x2 FMA
-                        const float2 x = __ffma2_rn(make_float2(s[2 * u], s[2 * u + 1]), sc2, nm2);
+                        const float2 x = __ffma2_rn(make_float2(s[c2][2 * u], s[c2][2 * u + 1]), sc2, nm2);
                         const float2 e2 = make_float2(ex2(x.x), ex2(x.y));
                         ps[u & 3] = __fadd2_rn(ps[u & 3], e2);
                         pw[c2 * 16 + u] = pack_bf16x2(e2.x, e2.y);
                     }
                 }
-                // P of keys [64 hh, 64 hh + 64) into columns [32 hh, 32 hh + 32): S there
-                // has been read already
-                tc::st_32words(sbase + hh * 32, pw);
-            }
+                tc::st_32words(sbase + hh * 64, pw);
+            };
+            weights(1);
+            load_half(0, s);
+            weights(0);
             tc::wait_st();
             const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
             const float2 pst = __fadd2_rn(ps01, ps23);
@@ -556,6 +556,7 @@ inline cudaError_t prefill_tc_prepare(void* out, const void* q, const void* k_po
         if (e != cudaSuccess) return e;
     }
     p.out = static_cast<__nv_bfloat16*>(out);
+    p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.cu_q_lens = cu_q_lens;

@@ -40,6 +40,25 @@ CASES = {
 }
 
 
+def _lengths(seed, B, q_lo, q_hi, c_lo, c_hi):
+    rng = np.random.default_rng(seed)
+    q = rng.integers(q_lo, q_hi + 1, size=B)
+    c = rng.integers(c_lo, c_hi + 1, size=B)
+    return list(map(int, q + c)), list(map(int, q))
+
+
+# Work-list cases of the persistent grid (each CTA runs a longest-first list of query
+# blocks): requests shorter than one query tile (items whose second tile is empty),
+# many items per CTA with prefixes of every length, and a batch past the list build's
+# request limit, which takes the one-CTA-per-block grid.
+_SQ, _QL = _lengths(5, 40, 1, 31, 0, 600)
+CASES["short_requests_many"] = (8, 2, 128, 16, _SQ, _QL)
+_SQ, _QL = _lengths(6, 24, 100, 260, 0, 900)
+CASES["several_blocks_per_cta"] = (32, 8, 128, 16, _SQ, _QL)
+_SQ, _QL = _lengths(7, 1030, 1, 1, 0, 40)
+CASES["requests_past_list_limit"] = (8, 2, 64, 16, _SQ, _QL)
+
+
 def _oracle_prefill(lay, vals, scale):
     kp, vp = oracle.build_pools(lay, vals)
     return oracle.paged_prefill(vals.q, kp, vp, lay.block_tables, lay.seq_lens, lay.cu_q_lens, scale,
