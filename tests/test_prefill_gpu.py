@@ -59,6 +59,11 @@ _SQ, _QL = _lengths(7, 1030, 1, 1, 0, 40)
 CASES["requests_past_list_limit"] = (8, 2, 64, 16, _SQ, _QL)
 
 
+# Every (D, G) instance of the one-CTA-per-query-block grid, which the standalone call
+# takes past the persistent grid's list limits (here: more than 1024 requests).
+LEGACY_GRID = [(64, 1), (64, 2), (64, 4), (64, 8), (128, 1), (128, 2), (128, 4), (128, 8)]
+
+
 def _oracle_prefill(lay, vals, scale):
     kp, vp = oracle.build_pools(lay, vals)
     return oracle.paged_prefill(vals.q, kp, vp, lay.block_tables, lay.seq_lens, lay.cu_q_lens, scale,
@@ -160,3 +165,19 @@ def test_prefill_flags_bad_lengths():
     ref = _oracle_prefill(lay, vals, 0.1)
     got = G.from_dev(out, W.BF16)
     G.assert_close(got[:10], ref[:10], W.BF16, "request 0 unaffected")
+
+
+@pytest.mark.parametrize("D,G", LEGACY_GRID)
+def test_prefill_one_cta_per_block_grid(D, G):
+    """1030 requests (past the persistent grid's request limit) of 1-3 new tokens on
+    cached prefixes of 0..40 positions, every (D, G) instance of the per-block grid."""
+    H_kv = 2
+    sl, ql = _lengths(100 + D + G, 1030, 1, 3, 0, 40)
+    lay = W.custom_layout(G * H_kv, H_kv, D, 16, W.BF16, sl, ql, seed=D * G)
+    vals = W.draw_layer_values(lay, np.random.default_rng(D + G))
+    scale = 1.0 / math.sqrt(D)
+    st = G.dev_status()
+    pools = G.build_dev_pools(lay, vals, st)
+    got = G.from_dev(G.run_prefill(lay, vals, pools, scale, st), W.BF16)
+    G.assert_close(got, _oracle_prefill(lay, vals, scale), W.BF16, f"per-block grid D={D} G={G}")
+    assert wf.wf_device_status_fetch(st) == 0
