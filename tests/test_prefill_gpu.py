@@ -167,17 +167,17 @@ def test_prefill_flags_bad_lengths():
     G.assert_close(got[:10], ref[:10], W.BF16, "request 0 unaffected")
 
 
-@pytest.mark.parametrize("D,G", LEGACY_GRID)
-def test_prefill_one_cta_per_block_grid(D, G):
+@pytest.mark.parametrize("D,grp", LEGACY_GRID)
+def test_prefill_one_cta_per_block_grid(D, grp):
     """1030 requests (past the persistent grid's request limit) of 1-3 new tokens on
     cached prefixes of 0..40 positions, every (D, G) instance of the per-block grid."""
     H_kv = 2
-    sl, ql = _lengths(100 + D + G, 1030, 1, 3, 0, 40)
-    lay = W.custom_layout(G * H_kv, H_kv, D, 16, W.BF16, sl, ql, seed=D * G)
-    vals = W.draw_layer_values(lay, np.random.default_rng(D + G))
+    sl, ql = _lengths(100 + D + grp, 1030, 1, 3, 0, 40)
+    lay = W.custom_layout(grp * H_kv, H_kv, D, 16, W.BF16, sl, ql, seed=D * grp)
+    vals = W.draw_layer_values(lay, np.random.default_rng(D + grp))
     scale = 1.0 / math.sqrt(D)
     st = G.dev_status()
     pools = G.build_dev_pools(lay, vals, st)
     got = G.from_dev(G.run_prefill(lay, vals, pools, scale, st), W.BF16)
-    G.assert_close(got, _oracle_prefill(lay, vals, scale), W.BF16, f"per-block grid D={D} G={G}")
+    G.assert_close(got, _oracle_prefill(lay, vals, scale), W.BF16, f"per-block grid D={D} G={grp}")
     assert wf.wf_device_status_fetch(st) == 0
