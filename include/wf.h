@@ -195,6 +195,11 @@ wf_status wf_paged_decode(void* out, const void* q, const void* k_pool, const vo
  *   max_q_len  >= every n_b (sizes the launch)
  * bfloat16 only; QK^T and PV run on the tensor cores (bf16 operands, fp32
  * accumulation in tensor memory); the softmax weights are rounded to bf16 for PV.
+ * Schedule (no effect on the result: the same bytes either way): a batch of at
+ * most 1024 requests and 4096 (request, query block) pairs -- a query block is
+ * 256 (token, query head) rows of one KV head -- runs as one persistent grid, one
+ * CTA per SM, each taking its share of the blocks longest first; a larger batch
+ * runs one CTA per query block.
  */
 wf_status wf_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                            const int32_t* block_tables, int32_t max_blocks_per_seq,
