@@ -67,6 +67,9 @@ CASES = {
     "gqa4_kv4_D64_P64": lambda: W.custom_layout(16, 4, 64, 64, W.BF16, [64, 65, 128, 129, 1000], seed=30),
     # a group of 8 stays on the CUDA cores
     "gqa8_bf16_cuda_cores": lambda: W.custom_layout(16, 2, 128, 16, W.BF16, [1, 300, 1029], seed=31),
+    # large blocks, up to the largest block size the calls accept (1024 positions)
+    "gqa4_D128_P256": lambda: W.custom_layout(32, 8, 128, 256, W.BF16, [1, 255, 256, 257, 1000, 3001], seed=32),
+    "gqa2_D64_P1024": lambda: W.custom_layout(16, 8, 64, 1024, W.BF16, [1, 1023, 1024, 1025, 2500], seed=33),
 }
 
 

@@ -37,6 +37,9 @@ CASES = {
     "D64_mha_gpt2": (12, 12, 64, 16, [300, 129, 40], [300, 64, 40]),
     "D64_gqa2": (16, 8, 64, 16, [520, 77], [260, 77]),
     "D64_gqa8": (16, 2, 64, 32, [333, 64, 1], [200, 64, 1]),
+    # large blocks, up to the largest block size the calls accept (1024 positions)
+    "P256_gqa4": (32, 8, 128, 256, [700, 300, 1], [300, 128, 1]),
+    "P1024_D64_gqa2": (16, 8, 64, 1024, [1500, 90], [700, 90]),
 }
 
 

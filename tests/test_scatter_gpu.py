@@ -26,6 +26,8 @@ def _layouts():
         "odd_P3_prefill": W.custom_layout(6, 3, 128, 3, W.BF16, [40, 7, 1], [5, 7, 1], seed=4),
         "P1_f32": W.custom_layout(4, 4, 64, 1, W.F32, [9, 3], seed=5),
         "P64_mha": W.custom_layout(12, 12, 64, 64, W.BF16, [100, 130, 64], seed=6),
+        "P256_gqa4": W.custom_layout(32, 8, 128, 256, W.BF16, [600, 1, 257], seed=7),
+        "P1024_largest_block": W.custom_layout(4, 2, 64, 1024, W.BF16, [1500, 3], seed=8),
     }
 
 
