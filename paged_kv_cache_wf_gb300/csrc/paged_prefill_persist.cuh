@@ -14,10 +14,15 @@
 //     (request, block) order -- expands each pair to its H_kv KV heads and deals the
 //     items to the CTAs in a snake (round r: CTA c takes item r * ncta + c, or
 //     r * ncta + ncta - 1 - c when r is odd), which balances the per-CTA work;
-//   * the producers stream the items' query tiles and K/V tiles through one ring
-//     without a break, so the next block's first tiles are in flight while the
-//     current block finishes, and the MMA warp issues the next block's first
-//     S = Q K^T while the softmax warps run the current block's epilogue.
+//   * a K warp and a V warp stream the items' K and V tiles through their rings
+//     without a break, and a third warp reloads each query tile as soon as its last
+//     S product of the previous item is done, so the next block's first tiles are in
+//     flight while the current block finishes, and the MMA warp issues the next
+//     block's first S = Q K^T while the softmax warps run the current block's
+//     epilogue;
+//   * the V tile an item ends in gets the rows of its last, partial 16-key block
+//     copied by hand (the rest zeroed) before it is handed over, so no warp waits
+//     for its own copy to land.
 // The ring's slots, the query tile and every barrier keep counting across items; each
 // role walks the same item list and derives every barrier phase from it.
 #pragma once
