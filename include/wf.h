@@ -358,6 +358,13 @@ typedef enum wf_kernel {
 } wf_kernel;
 int wf_paged_decode_kernel(wf_pool_desc pool, int32_t num_q_heads);
 int wf_paged_prefill_kernel(wf_pool_desc pool, int32_t num_q_heads);
+/*
+ * 1 when wf_paged_prefill runs a batch of B requests of at most max_q_len new tokens
+ * as the persistent grid (WF_KERNEL_TENSOR_CORES geometries within the work list's
+ * limits: B <= 1024 and B * ceil(max_q_len / query block) <= 4096), 0 when it runs one
+ * CTA per query block (or the geometry is not WF_KERNEL_TENSOR_CORES).  Host-only.
+ */
+int wf_paged_prefill_persistent(wf_pool_desc pool, int32_t num_q_heads, int32_t B, int32_t max_q_len);
 
 /*
  * Wait for `stream`, copy *dev_status to *host_status and, if clear != 0, reset

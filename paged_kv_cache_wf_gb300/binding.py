@@ -32,6 +32,7 @@ EXPORTS = (
     "wf_decode_worker",
     "wf_paged_decode_kernel",
     "wf_paged_prefill_kernel",
+    "wf_paged_prefill_persistent",
     "wf_device_status_fetch",
     "wf_status_string",
     "wf_abi_version",
@@ -101,6 +102,8 @@ def load(path: str = LIB_PATH):
         lib.wf_paged_decode_kernel.restype = ctypes.c_int
         lib.wf_paged_prefill_kernel.argtypes = [wf_pool_desc, i32]
         lib.wf_paged_prefill_kernel.restype = ctypes.c_int
+        lib.wf_paged_prefill_persistent.argtypes = [wf_pool_desc, i32, i32, i32]
+        lib.wf_paged_prefill_persistent.restype = ctypes.c_int
         lib.wf_device_status_fetch.argtypes = [vp, vp, ctypes.c_int, vp]
         lib.wf_device_status_fetch.restype = ctypes.c_int
         lib.wf_status_string.argtypes = [ctypes.c_int]
@@ -322,6 +325,11 @@ def wf_paged_decode_kernel(desc: wf_pool_desc, num_q_heads: int) -> int:
 def wf_paged_prefill_kernel(desc: wf_pool_desc, num_q_heads: int) -> int:
     """The WF_KERNEL_* value of the kernel wf_paged_prefill runs for this geometry."""
     return int(load().wf_paged_prefill_kernel(desc, int(num_q_heads)))
+
+
+def wf_paged_prefill_persistent(desc: wf_pool_desc, num_q_heads: int, B: int, max_q_len: int) -> bool:
+    """Whether wf_paged_prefill runs a batch of this shape as its persistent grid."""
+    return bool(load().wf_paged_prefill_persistent(desc, int(num_q_heads), int(B), int(max_q_len)))
 
 
 def wf_device_status_fetch(dev_status, clear: bool = True, stream=None) -> int:

@@ -116,7 +116,7 @@ wf_status from_cuda(cudaError_t e) {
 
 extern "C" {
 
-int wf_abi_version(void) { return 103; }
+int wf_abi_version(void) { return 104; }
 
 const char* wf_status_string(wf_status s) {
     switch (s) {
@@ -319,6 +319,12 @@ int wf_paged_decode_kernel(wf_pool_desc pool, int32_t num_q_heads) {
 int wf_paged_prefill_kernel(wf_pool_desc pool, int32_t num_q_heads) {
     if (check_pool(pool) != WF_OK || num_q_heads < 1) return WF_KERNEL_NONE;
     return wf::prefill_kernel_kind(pool, num_q_heads);
+}
+
+int wf_paged_prefill_persistent(wf_pool_desc pool, int32_t num_q_heads, int32_t B, int32_t max_q_len) {
+    if (check_pool(pool) != WF_OK || num_q_heads < 1) return 0;
+    if (wf::prefill_kernel_kind(pool, num_q_heads) != WF_KERNEL_TENSOR_CORES) return 0;
+    return wf::prefill_tc_persistent(pool, num_q_heads, B, max_q_len) ? 1 : 0;
 }
 
 wf_status wf_device_status_fetch(uint32_t* dev_status, uint32_t* host_status, int clear,

@@ -155,6 +155,8 @@ cudaError_t launch_paged_prefill_tc(void* out, const void* q, const void* k_pool
 
 // The wf_kernel value of the prefill kernel launch_paged_prefill picks.
 int prefill_kernel_kind(const wf_pool_desc& pool, int32_t num_q_heads);
+// Whether the pipelined tensor-core prefill runs this batch shape as its persistent grid.
+bool prefill_tc_persistent(const wf_pool_desc& pool, int32_t num_q_heads, int32_t B, int32_t max_q_len);
 cudaError_t launch_paged_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
                                  const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,

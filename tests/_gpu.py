@@ -33,6 +33,11 @@ def prefill_kernel(geom) -> int:
     return wf.wf_paged_prefill_kernel(geom_desc(geom), geom.H_q)
 
 
+def prefill_persistent(lay) -> bool:
+    """Whether wf_paged_prefill runs this batch as the persistent grid."""
+    return wf.wf_paged_prefill_persistent(geom_desc(lay.geom), lay.geom.H_q, lay.B, lay.max_q_len)
+
+
 def torch_mod():
     import torch
     return torch

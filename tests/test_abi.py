@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.wf_abi_version() == 103
+    assert lib.wf_abi_version() == 104
     for code in range(6):
         assert wf.status_string(code)
 

@@ -72,6 +72,45 @@ def test_prefill_cases_reach_every_tensor_core_instance(lib):
     assert simple >= 2
 
 
+def test_prefill_cases_reach_both_grids(lib):
+    """The prefill cases run the persistent grid at every (G, D) instance, and the
+    one-CTA-per-block grid (the list build's limits exceeded) at every instance too."""
+    from paged_kv_cache_wf_gb300 import workloads as W
+    from tests import test_prefill_gpu as T
+    persistent, per_block = set(), set()
+    for name, (H_q, H_kv, D, P, sl, ql) in T.CASES.items():
+        lay = W.custom_layout(H_q, H_kv, D, P, W.BF16, sl, ql, seed=len(name))
+        if G.prefill_kernel(lay.geom) != wf.WF_KERNEL_TENSOR_CORES:
+            continue
+        (persistent if G.prefill_persistent(lay) else per_block).add((H_q // H_kv, D))
+    for D, grp in T.LEGACY_GRID:
+        lay = T.legacy_grid_layout(D, grp)
+        assert G.prefill_kernel(lay.geom) == wf.WF_KERNEL_TENSOR_CORES
+        assert not G.prefill_persistent(lay)
+        per_block.add((grp, D))
+    want = {(gs, d) for gs in (1, 2, 4, 8) for d in (64, 128)}
+    assert want <= persistent, want - persistent
+    assert want <= per_block, want - per_block
+
+
+def test_prefill_grid_query_limits(lib):
+    """The list build takes up to 1024 requests and 4096 (request, query block) pairs;
+    the query answers 0 for what the per-block grid or no tensor-core kernel runs."""
+    d = wf.wf_pool_desc(64, 16, 8, 128, wf.WF_DTYPE_BF16, 1.0, 1.0)
+    assert wf.wf_paged_prefill_persistent(d, 32, 1, 1)
+    assert wf.wf_paged_prefill_persistent(d, 32, 1024, 1)
+    assert not wf.wf_paged_prefill_persistent(d, 32, 1025, 1)
+    assert not wf.wf_paged_prefill_persistent(d, 32, 0, 1)
+    # G = 4: 256-row query blocks of 64 positions; 64 requests x 64 blocks = 4096 pairs
+    assert wf.wf_paged_prefill_persistent(d, 32, 64, 64 * 64)
+    assert not wf.wf_paged_prefill_persistent(d, 32, 64, 64 * 64 + 1)
+    d.block_size = 8                                             # not a multiple of 16
+    assert not wf.wf_paged_prefill_persistent(d, 32, 4, 100)
+    d.block_size = 16
+    d.dtype = wf.WF_DTYPE_FP8_E4M3                               # prefill is bf16 only
+    assert not wf.wf_paged_prefill_persistent(d, 32, 4, 100)
+
+
 def test_kernel_query_rejects_invalid_geometry(lib):
     d = wf.wf_pool_desc(16, 16, 8, 96, wf.WF_DTYPE_BF16, 1.0, 1.0)
     assert wf.wf_paged_decode_kernel(d, 32) == wf.WF_KERNEL_NONE

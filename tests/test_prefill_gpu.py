@@ -170,13 +170,19 @@ def test_prefill_flags_bad_lengths():
     G.assert_close(got[:10], ref[:10], W.BF16, "request 0 unaffected")
 
 
-@pytest.mark.parametrize("D,grp", LEGACY_GRID)
-def test_prefill_one_cta_per_block_grid(D, grp):
+def legacy_grid_layout(D, grp):
     """1030 requests (past the persistent grid's request limit) of 1-3 new tokens on
-    cached prefixes of 0..40 positions, every (D, G) instance of the per-block grid."""
+    cached prefixes of 0..40 positions."""
     H_kv = 2
     sl, ql = _lengths(100 + D + grp, 1030, 1, 3, 0, 40)
-    lay = W.custom_layout(grp * H_kv, H_kv, D, 16, W.BF16, sl, ql, seed=D * grp)
+    return W.custom_layout(grp * H_kv, H_kv, D, 16, W.BF16, sl, ql, seed=D * grp)
+
+
+@pytest.mark.parametrize("D,grp", LEGACY_GRID)
+def test_prefill_one_cta_per_block_grid(D, grp):
+    """Every (D, G) instance of the per-block grid on a batch past the list limits."""
+    lay = legacy_grid_layout(D, grp)
+    assert not G.prefill_persistent(lay)
     vals = W.draw_layer_values(lay, np.random.default_rng(D + grp))
     scale = 1.0 / math.sqrt(D)
     st = G.dev_status()
