@@ -24,6 +24,7 @@
 //     MN-major operand -- no transpose pass.  The epilogue reads O from TMEM,
 //     divides by the row sum and stores bf16.
 #include "wf_internal.h"
+#include "paged_prefill_persist.cuh"
 
 namespace wf {
 
@@ -276,6 +277,27 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+bool prefill_tc_persistent(const wf_pool_desc& pool, int32_t num_q_heads, int32_t B, int32_t max_q_len) {
+    if (!prefill_tc_supported(pool, num_q_heads) || B < 1 || max_q_len < 1) return false;
+    const int G = num_q_heads / pool.num_kv_heads;
+    const int H_kv = pool.num_kv_heads;
+    // the grid's yes / no does not depend on the SM count (1 here)
+    if (pool.head_dim == 128) {
+        switch (G) {
+            case 1: return prefill_persist_grid<128, 1>(B, max_q_len, H_kv, 1) > 0;
+            case 2: return prefill_persist_grid<128, 2>(B, max_q_len, H_kv, 1) > 0;
+            case 4: return prefill_persist_grid<128, 4>(B, max_q_len, H_kv, 1) > 0;
+            default: return prefill_persist_grid<128, 8>(B, max_q_len, H_kv, 1) > 0;
+        }
+    }
+    switch (G) {
+        case 1: return prefill_persist_grid<64, 1>(B, max_q_len, H_kv, 1) > 0;
+        case 2: return prefill_persist_grid<64, 2>(B, max_q_len, H_kv, 1) > 0;
+        case 4: return prefill_persist_grid<64, 4>(B, max_q_len, H_kv, 1) > 0;
+        default: return prefill_persist_grid<64, 8>(B, max_q_len, H_kv, 1) > 0;
+    }
+}
 
 int prefill_kernel_kind(const wf_pool_desc& pool, int32_t num_q_heads) {
     if (pool.dtype != WF_DTYPE_BF16 || (pool.head_dim != 64 && pool.head_dim != 128)) return WF_KERNEL_NONE;

@@ -56,27 +56,6 @@ bool prefill_tc_supported(const wf_pool_desc& pool, int32_t num_q_heads) {
     return G == 1 || G == 2 || G == 4 || G == 8;
 }
 
-bool prefill_tc_persistent(const wf_pool_desc& pool, int32_t num_q_heads, int32_t B, int32_t max_q_len) {
-    if (!prefill_tc_supported(pool, num_q_heads) || B < 1 || max_q_len < 1) return false;
-    const int G = num_q_heads / pool.num_kv_heads;
-    const int H_kv = pool.num_kv_heads;
-    // the grid's yes / no does not depend on the SM count (1 here)
-    if (pool.head_dim == 128) {
-        switch (G) {
-            case 1: return prefill_persist_grid<128, 1>(B, max_q_len, H_kv, 1) > 0;
-            case 2: return prefill_persist_grid<128, 2>(B, max_q_len, H_kv, 1) > 0;
-            case 4: return prefill_persist_grid<128, 4>(B, max_q_len, H_kv, 1) > 0;
-            default: return prefill_persist_grid<128, 8>(B, max_q_len, H_kv, 1) > 0;
-        }
-    }
-    switch (G) {
-        case 1: return prefill_persist_grid<64, 1>(B, max_q_len, H_kv, 1) > 0;
-        case 2: return prefill_persist_grid<64, 2>(B, max_q_len, H_kv, 1) > 0;
-        case 4: return prefill_persist_grid<64, 4>(B, max_q_len, H_kv, 1) > 0;
-        default: return prefill_persist_grid<64, 8>(B, max_q_len, H_kv, 1) > 0;
-    }
-}
-
 cudaError_t launch_paged_prefill_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
                                     const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t B,
